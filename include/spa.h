@@ -1,0 +1,136 @@
+/*
+ * spa.h -- C ABI of the GB300 (sm_103a) projected-feature softmax attention
+ * library, libspa.so.
+ *
+ * The operation (per batch b and head h):
+ *     Qp = Q P_h,  Kp = K P_h                P_h in R^{d x m}
+ *     O  = softmax( Qp Kp^T / sqrt(m) ) V    row-wise softmax, full N x N
+ * as defined by "Sparse Projection Attention: A Computationally Efficient
+ * Framework for Long Sequence Modeling" (Sec. 3.1.2, Sec. 3.1.3, Algorithm 1)
+ * and by steps 1-3 of Algorithm 2.1 of the "Projection-Decomposition
+ * Attention" page (steps 4-5, the rank-r factorisation, are not part of this
+ * library).  With causal != 0 query i only attends to keys j <= i (square,
+ * top-left aligned mask).
+ *
+ * Conventions shared by every entry point
+ *   Layout     all tensors dense, row-major, no padding:
+ *                q, k   [B][H][N][d]      v, out  [B][H][N][d_v]
+ *                P      [H][d][m]         one projection per head, shared by all b
+ *   dtype      SPA_F32 or SPA_BF16; q, k, v and P all have this element type.
+ *              Outputs are always fp32.
+ *   Memory     unless an entry point says otherwise, every pointer is a CUDA
+ *              device pointer on the current device, 16-byte aligned.  The
+ *              caller owns every buffer; the library keeps no device memory
+ *              between calls.
+ *   stream     a cudaStream_t passed as void* (NULL = legacy default stream).
+ *              Work is enqueued asynchronously; the return value reports
+ *              argument errors and launch errors only.  Faults inside a kernel
+ *              surface at the caller's next synchronisation.
+ *   Empty      if B*H*N == 0 the call returns SPA_OK and touches nothing.
+ *   Errors     a non-zero return is an spa_status; nothing was enqueued unless
+ *              the status is SPA_ERR_CUDA from a launch.
+ *   Threads    all entry points are reentrant.
+ */
+#ifndef SPA_H
+#define SPA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPA_OK = 0,
+  SPA_ERR_NULL = 1,        /* a required pointer is NULL                      */
+  SPA_ERR_SHAPE = 2,       /* a size is negative or too large                 */
+  SPA_ERR_DTYPE = 3,       /* dtype is not SPA_F32 / SPA_BF16                 */
+  SPA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned                */
+  SPA_ERR_UNSUPPORTED = 5, /* shape outside what the kernels implement        */
+  SPA_ERR_NOMEM = 6,       /* workspace allocation failed / too small         */
+  SPA_ERR_CUDA = 7,        /* a CUDA runtime or driver call failed            */
+  SPA_ERR_TIMEOUT = 8      /* a kernel gave up on a bounded wait (device word) */
+} spa_status;
+
+typedef enum { SPA_F32 = 0, SPA_BF16 = 1 } spa_dtype;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *spa_status_str(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int spa_version(void);
+
+/*
+ * spa_project -- the projection step alone: x_proj[b][h][i][:] = x[b][h][i][:] P_h
+ * (SPA Algorithm 1 steps 2-3; PDA Algorithm 2.1 step 1).
+ *   x       [B][H][N][d] of `dtype`, device.
+ *   P       [H][d][m] of `dtype`, device.
+ *   x_proj  [B][H][N][m] fp32, device, written.
+ * Products of the inputs are formed exactly and summed in fp32.
+ * Supported: 1 <= d <= 256, 1 <= m <= 128.
+ */
+int spa_project(const void *x, const void *P, float *x_proj, int B, int H, int N, int d, int m,
+                int dtype, void *stream);
+
+/*
+ * spa_attention_fwd -- the whole forward: projection, scores, (causal mask),
+ * online softmax and the value product, without forming the N x N matrix.
+ *   q, k    [B][H][N][d] of `dtype`, device.
+ *   v       [B][H][N][d_v] of `dtype`, device.
+ *   P       [H][d][m] of `dtype`, device.
+ *   out     [B][H][N][d_v] fp32, device, written.
+ *   causal  0 = full attention, non-zero = key j visible to query i iff j <= i.
+ * Supported:
+ *   SPA_BF16: 1 <= d <= 256; m in {16, 32, 64, 128}; d_v in {64, 128}.
+ *   SPA_F32 : 1 <= d <= 256; 1 <= m <= 128;          1 <= d_v <= 256.
+ *   N up to 2^31 - 1, B*H up to 65535.
+ * A workspace of spa_attention_workspace_size() bytes is taken with
+ * cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
+ * stream (SPA_ERR_NOMEM if the allocation fails).
+ */
+int spa_attention_fwd(const void *q, const void *k, const void *v, const void *P, float *out,
+                      int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                      void *stream);
+
+/*
+ * spa_attention_workspace_size -- bytes of device workspace the forward needs
+ * for these sizes (0 when B*H*N == 0).  Validates like spa_attention_fwd.
+ */
+int spa_attention_workspace_size(int B, int H, int N, int d, int m, int d_v, int dtype,
+                                 size_t *bytes);
+
+/*
+ * spa_attention_fwd_ws -- spa_attention_fwd with a caller-provided workspace
+ * (device, 256-byte aligned, at least spa_attention_workspace_size() bytes;
+ * SPA_ERR_NOMEM if smaller).  The workspace is overwritten; it must not be in
+ * use by other work on other streams while this call's kernels run.
+ */
+int spa_attention_fwd_ws(const void *q, const void *k, const void *v, const void *P, float *out,
+                         int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spa_attention_fwd_host -- end-to-end form on HOST buffers: copies q, k, v, P
+ * to the device, runs the forward, copies out back, and synchronises `stream`
+ * before returning, so `out` is valid on return.  Device buffers and the
+ * workspace are taken with cudaMallocAsync and released before return.
+ * Page-locked host buffers give asynchronous, full-bandwidth copies; pageable
+ * ones work but copy synchronously.  Same shapes and dtypes as
+ * spa_attention_fwd.
+ */
+int spa_attention_fwd_host(const void *q, const void *k, const void *v, const void *P,
+                           float *out, int B, int H, int N, int d, int m, int d_v, int causal,
+                           int dtype, void *stream);
+
+/*
+ * spa_device_error -- reads and clears the device error word of the current
+ * device (synchronising it first).  *code receives 0 when no kernel gave up
+ * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.
+ */
+int spa_device_error(int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPA_H */

@@ -1,0 +1,23 @@
+"""GB300 (sm_103a) projected-feature softmax attention.
+
+    Qp = Q P_h,  Kp = K P_h,  O = softmax(Qp Kp^T / sqrt(m)) V
+
+Thin Python binding of ``libspa.so`` (C ABI in include/spa.h).  The binding
+only marshals torch tensors into pointers and sizes; every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: the
+first use of any binding name loads ``libspa.so`` and raises ImportError if it
+has not been built (``python -m projected_feature_efficient_gb300.build``).
+"""
+import importlib
+
+__all__ = [
+    "SPA_BF16", "SPA_F32", "SpaError", "device_error", "lib", "lib_path",
+    "spa_attention_fwd", "spa_attention_fwd_host", "spa_attention_fwd_ws",
+    "spa_attention_workspace_size", "spa_project", "status_str",
+]
+
+
+def __getattr__(name):
+    if name in __all__:
+        return getattr(importlib.import_module("._binding", __name__), name)
+    raise AttributeError(name)

@@ -1,0 +1,153 @@
+"""ctypes binding of libspa.so: argument marshalling only.
+
+Torch tensors supply data pointers, shapes and the current CUDA stream; the
+functions raise ``SpaError`` on any non-zero status.  Names follow the C ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libspa.so")
+
+if not os.path.exists(lib_path):
+    raise ImportError(
+        f"libspa.so is not built ({lib_path}); build it with "
+        "`python -m projected_feature_efficient_gb300.build` (needs nvcc)")
+
+lib = ctypes.CDLL(lib_path)
+
+SPA_F32, SPA_BF16 = 0, 1
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+lib.spa_status_str.argtypes = [_i]
+lib.spa_status_str.restype = ctypes.c_char_p
+lib.spa_version.argtypes = []
+lib.spa_version.restype = _i
+lib.spa_project.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
+lib.spa_project.restype = _i
+lib.spa_attention_fwd.argtypes = [_vp] * 5 + [_i] * 8 + [_vp]
+lib.spa_attention_fwd.restype = _i
+lib.spa_attention_workspace_size.argtypes = [_i] * 7 + [ctypes.POINTER(_sz)]
+lib.spa_attention_workspace_size.restype = _i
+lib.spa_attention_fwd_ws.argtypes = [_vp] * 5 + [_i] * 8 + [_vp, _sz, _vp]
+lib.spa_attention_fwd_ws.restype = _i
+lib.spa_attention_fwd_host.argtypes = [_vp] * 5 + [_i] * 8 + [_vp]
+lib.spa_attention_fwd_host.restype = _i
+lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
+lib.spa_device_error.restype = _i
+
+
+class SpaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)}")
+
+
+def status_str(status: int) -> str:
+    return lib.spa_status_str(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SpaError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SPA_BF16
+    if t.dtype == torch.float32:
+        return SPA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _shapes(q, k, v, P):
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    m = P.shape[-1]
+    if tuple(k.shape) != (B, H, N, d) or tuple(v.shape) != (B, H, N, dv) or \
+            tuple(P.shape) != (H, d, m):
+        raise ValueError("shapes: q,k [B,H,N,d]; v [B,H,N,dv]; P [H,d,m]")
+    for t in (q, k, v, P):
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    if len({t.dtype for t in (q, k, v, P)}) != 1:
+        raise TypeError("q, k, v and P must share one dtype")
+    return B, H, N, d, m, dv
+
+
+def spa_project(x, P, out=None, stream=None):
+    """x [B,H,N,d] @ P [H,d,m] -> fp32 [B,H,N,m] (device tensors)."""
+    import torch
+    B, H, N, d = x.shape
+    m = P.shape[-1]
+    if tuple(P.shape) != (H, d, m) or x.dtype != P.dtype:
+        raise ValueError("P must be [H,d,m] with x's dtype")
+    if out is None:
+        out = torch.empty((B, H, N, m), dtype=torch.float32, device=x.device)
+    _check(lib.spa_project(_ptr(x), _ptr(P), _ptr(out), B, H, N, d, m, _dtype_code(x),
+                           _stream_ptr(stream)), "spa_project")
+    return out
+
+
+def spa_attention_fwd(q, k, v, P, causal=False, out=None, stream=None):
+    """Forward on device tensors; returns fp32 [B,H,N,dv]."""
+    import torch
+    B, H, N, d, m, dv = _shapes(q, k, v, P)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    _check(lib.spa_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), B, H, N, d, m,
+                                 dv, int(bool(causal)), _dtype_code(q), _stream_ptr(stream)),
+           "spa_attention_fwd")
+    return out
+
+
+def spa_attention_workspace_size(B, H, N, d, m, dv, dtype_code) -> int:
+    n = _sz(0)
+    _check(lib.spa_attention_workspace_size(B, H, N, d, m, dv, dtype_code, ctypes.byref(n)),
+           "spa_attention_workspace_size")
+    return int(n.value)
+
+
+def spa_attention_fwd_ws(q, k, v, P, workspace, causal=False, out=None, stream=None):
+    """Forward with a caller-provided device workspace (uint8 tensor)."""
+    import torch
+    B, H, N, d, m, dv = _shapes(q, k, v, P)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    _check(lib.spa_attention_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), B, H, N, d, m,
+                                    dv, int(bool(causal)), _dtype_code(q), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream_ptr(stream)), "spa_attention_fwd_ws")
+    return out
+
+
+def spa_attention_fwd_host(q, k, v, P, causal=False, out=None, stream=None):
+    """End-to-end form on host (CPU) tensors: copies in, computes, copies out."""
+    import torch
+    B, H, N, d, m, dv = _shapes(q, k, v, P)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32)
+    _check(lib.spa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), B, H, N, d,
+                                      m, dv, int(bool(causal)), _dtype_code(q),
+                                      _stream_ptr(stream)), "spa_attention_fwd_host")
+    return out
+
+
+def device_error() -> int:
+    """Read and clear the device error word (0 or SPA_ERR_TIMEOUT)."""
+    c = _i(0)
+    _check(lib.spa_device_error(ctypes.byref(c)), "spa_device_error")
+    return int(c.value)

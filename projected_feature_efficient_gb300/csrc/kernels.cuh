@@ -1,0 +1,61 @@
+// kernels.cuh -- host-side launchers shared between the C ABI (spa_api.cu)
+// and the kernel translation units.  Internal to libspa.so.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace spa {
+
+// How the projection writes its result.
+enum class ProjOut : int {
+  F32 = 0,       // plain fp32 rows [BH][N][m]
+  F16X1 = 1,     // fp16 UMMA tiles, power-of-two row (Q) / tile (K) exponents
+  BF16X3 = 2,    // bf16 hi/lo split UMMA tiles, depth 3m
+};
+
+// Score-GEMM operand tiles: 128 rows x KD columns of 16-bit values in the
+// interleaved K-major core-matrix layout the tensor cores read directly:
+//   element (r, k) of a tile sits at ((k/8)*16 + r/8)*64 + (r%8)*8 + k%8.
+constexpr int kTileRows = 128;
+
+inline int score_depth(int m, ProjOut mode) { return mode == ProjOut::BF16X3 ? 3 * m : m; }
+
+struct ProjParams {
+  const void* x[2];      // [BH][N][d] inputs (Q-like at 0, K-like at 1)
+  const void* P;         // [H][d][m]
+  void* out[2];          // F32: [BH][N][m] float; tiles: [BH][NT][128*KD] u16
+  float* mul[2];         // tiles: Q row multipliers [BH][NT*128], K tile multipliers [BH][NT]
+  int nx;                // 1 or 2 tensors
+  int BH, H, N, d, m, NT;
+  float qscale;          // factor folded into tensor 0 before conversion (tile modes)
+  int bf16_in;           // element type of x and P: 1 = bf16, 0 = fp32
+  ProjOut mode;
+};
+cudaError_t launch_project(const ProjParams& p, cudaStream_t stream);
+
+struct AttnTcParams {
+  const uint16_t* Qs;    // [BH][NT][128*KD]
+  const uint16_t* Ks;    // [BH][NT][128*KD]
+  const float* qmul;     // [BH][NT*128]
+  const float* kmul;     // [BH][NT]
+  CUtensorMap vmap;      // V as 3-D (d_v, N, BH), bf16, 128-byte swizzle, box (64,128,1)
+  float* out;            // [BH][N][d_v]
+  int* err;              // device error word
+  int BH, N, NT, KD, dv, causal;
+  int f16_ops;           // 1: fp16 score operands, 0: bf16
+};
+cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t stream);
+
+struct AttnF32Params {
+  const float* Qp;       // [BH][N][m]
+  const float* Kp;       // [BH][N][m]
+  const float* V;        // [BH][N][dv]
+  float* out;            // [BH][N][dv]
+  int BH, N, m, dv, causal;
+  float scale;           // 1/sqrt(m)
+};
+cudaError_t launch_attn_f32(const AttnF32Params& p, cudaStream_t stream);
+
+}  // namespace spa

@@ -1,0 +1,340 @@
+// spa_api.cu -- the C ABI of libspa.so (declared in include/spa.h): argument
+// validation, workspace layout, tensor-map encoding, launches and status codes.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/spa.h"
+#include "kernels.cuh"
+
+namespace {
+
+using spa::ProjOut;
+
+// Device word set by a kernel that gave up on a bounded wait.
+__device__ int g_spa_device_error;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+int device_error_ptr(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_spa_device_error) != cudaSuccess) return SPA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return SPA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  *fn = g_encode;
+  return g_encode ? SPA_OK : SPA_ERR_CUDA;
+}
+
+constexpr int kEmpty = -1;  // internal: nothing to do
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape / dtype checks shared by every forward entry point.
+int check_shape(int B, int H, int N, int d, int m, int dv, int dtype) {
+  if (B < 0 || H < 0 || N < 0 || d < 0 || m < 0 || dv < 0) return SPA_ERR_SHAPE;
+  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
+  if (static_cast<long long>(B) * H * N == 0) return kEmpty;
+  if (static_cast<long long>(B) * H > 65535) return SPA_ERR_SHAPE;
+  if (d < 1 || d > 256 || m < 1 || m > 128 || dv < 1 || dv > 256) return SPA_ERR_UNSUPPORTED;
+  if (dtype == SPA_BF16) {
+    if (m != 16 && m != 32 && m != 64 && m != 128) return SPA_ERR_UNSUPPORTED;
+    if (dv != 64 && dv != 128) return SPA_ERR_UNSUPPORTED;
+  }
+  return SPA_OK;
+}
+
+struct Layout {
+  int NT = 0, KD = 0;
+  ProjOut mode = ProjOut::F32;
+  size_t qs = 0, ks = 0, qmul = 0, kmul = 0;  // bf16 path
+  size_t qp = 0, kp = 0;                      // fp32 path
+  size_t total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Layout make_layout(int B, int H, int N, int m, int dtype) {
+  Layout L;
+  const size_t BH = static_cast<size_t>(B) * H;
+  if (dtype == SPA_BF16) {
+    L.NT = (N + spa::kTileRows - 1) / spa::kTileRows;
+    L.mode = m == 16 ? ProjOut::BF16X3 : ProjOut::F16X1;
+    L.KD = spa::score_depth(m, L.mode);
+    const size_t tiles = BH * L.NT * spa::kTileRows * L.KD * 2;
+    L.qs = 0;
+    L.ks = align256(L.qs + tiles);
+    L.qmul = align256(L.ks + tiles);
+    L.kmul = align256(L.qmul + BH * L.NT * spa::kTileRows * sizeof(float));
+    L.total = align256(L.kmul + BH * L.NT * sizeof(float));
+  } else {
+    const size_t proj = BH * N * m * sizeof(float);
+    L.qp = 0;
+    L.kp = align256(proj);
+    L.total = align256(L.kp + proj);
+  }
+  return L;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPA_OK : SPA_ERR_CUDA; }
+
+int run_forward(const void* q, const void* k, const void* v, const void* P, float* out, int B,
+                int H, int N, int d, int m, int dv, int causal, int dtype, void* ws,
+                cudaStream_t stream) {
+  const Layout L = make_layout(B, H, N, m, dtype);
+  const int BH = B * H;
+  char* w = static_cast<char*>(ws);
+  spa::ProjParams pp{};
+  pp.x[0] = q;
+  pp.x[1] = k;
+  pp.P = P;
+  pp.nx = 2;
+  pp.BH = BH;
+  pp.H = H;
+  pp.N = N;
+  pp.d = d;
+  pp.m = m;
+  pp.bf16_in = dtype == SPA_BF16;
+
+  if (dtype == SPA_F32) {
+    pp.mode = ProjOut::F32;
+    pp.out[0] = w + L.qp;
+    pp.out[1] = w + L.kp;
+    pp.NT = (N + spa::kTileRows - 1) / spa::kTileRows;
+    int st = cuda_status(spa::launch_project(pp, stream));
+    if (st) return st;
+    spa::AttnF32Params ap{};
+    ap.Qp = reinterpret_cast<const float*>(w + L.qp);
+    ap.Kp = reinterpret_cast<const float*>(w + L.kp);
+    ap.V = static_cast<const float*>(v);
+    ap.out = out;
+    ap.BH = BH;
+    ap.N = N;
+    ap.m = m;
+    ap.dv = dv;
+    ap.causal = causal != 0;
+    ap.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
+    return cuda_status(spa::launch_attn_f32(ap, stream));
+  }
+
+  pp.mode = L.mode;
+  pp.NT = L.NT;
+  pp.out[0] = w + L.qs;
+  pp.out[1] = w + L.ks;
+  pp.mul[0] = reinterpret_cast<float*>(w + L.qmul);
+  pp.mul[1] = reinterpret_cast<float*>(w + L.kmul);
+  // scores come out in base-2 logits: fold log2(e) / sqrt(m) into Q
+  pp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m)));
+  int st = cuda_status(spa::launch_project(pp, stream));
+  if (st) return st;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  if ((st = get_encode(&encode))) return st;
+  spa::AttnTcParams ap{};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dv) * 2,
+                           static_cast<cuuint64_t>(N) * dv * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(spa::kTileRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (encode(&ap.vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SPA_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_error_ptr(&err))) return st;
+  ap.Qs = reinterpret_cast<const uint16_t*>(w + L.qs);
+  ap.Ks = reinterpret_cast<const uint16_t*>(w + L.ks);
+  ap.qmul = reinterpret_cast<const float*>(w + L.qmul);
+  ap.kmul = reinterpret_cast<const float*>(w + L.kmul);
+  ap.out = out;
+  ap.err = err;
+  ap.BH = BH;
+  ap.N = N;
+  ap.NT = L.NT;
+  ap.KD = L.KD;
+  ap.dv = dv;
+  ap.causal = causal != 0;
+  ap.f16_ops = L.mode == ProjOut::F16X1;
+  return cuda_status(spa::launch_attn_tc(ap, stream));
+}
+
+int check_forward_ptrs(const void* q, const void* k, const void* v, const void* P,
+                       const void* out) {
+  if (!q || !k || !v || !P || !out) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(P) || !aligned16(out))
+    return SPA_ERR_ALIGN;
+  return SPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spa_status_str(int status) {
+  switch (status) {
+    case SPA_OK: return "SPA_OK";
+    case SPA_ERR_NULL: return "SPA_ERR_NULL: a required pointer is NULL";
+    case SPA_ERR_SHAPE: return "SPA_ERR_SHAPE: a size is negative or too large";
+    case SPA_ERR_DTYPE: return "SPA_ERR_DTYPE: dtype must be SPA_F32 or SPA_BF16";
+    case SPA_ERR_ALIGN: return "SPA_ERR_ALIGN: pointers must be 16-byte aligned";
+    case SPA_ERR_UNSUPPORTED: return "SPA_ERR_UNSUPPORTED: shape outside the implemented kernels";
+    case SPA_ERR_NOMEM: return "SPA_ERR_NOMEM: workspace allocation failed or too small";
+    case SPA_ERR_CUDA: return "SPA_ERR_CUDA: a CUDA call failed";
+    case SPA_ERR_TIMEOUT: return "SPA_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    default: return "SPA_ERR_UNKNOWN";
+  }
+}
+
+int spa_version(void) { return 100; }
+
+int spa_project(const void* x, const void* P, float* x_proj, int B, int H, int N, int d, int m,
+                int dtype, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || d < 0 || m < 0) return SPA_ERR_SHAPE;
+  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
+  if (static_cast<long long>(B) * H * N == 0) return SPA_OK;
+  if (static_cast<long long>(B) * H > 65535) return SPA_ERR_SHAPE;
+  if (d < 1 || d > 256 || m < 1 || m > 128) return SPA_ERR_UNSUPPORTED;
+  if (!x || !P || !x_proj) return SPA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(P) || !aligned16(x_proj)) return SPA_ERR_ALIGN;
+  spa::ProjParams pp{};
+  pp.x[0] = x;
+  pp.P = P;
+  pp.out[0] = x_proj;
+  pp.nx = 1;
+  pp.BH = B * H;
+  pp.H = H;
+  pp.N = N;
+  pp.d = d;
+  pp.m = m;
+  pp.NT = (N + spa::kTileRows - 1) / spa::kTileRows;
+  pp.bf16_in = dtype == SPA_BF16;
+  pp.mode = ProjOut::F32;
+  return cuda_status(spa::launch_project(pp, static_cast<cudaStream_t>(stream)));
+}
+
+int spa_attention_workspace_size(int B, int H, int N, int d, int m, int d_v, int dtype,
+                                 size_t* bytes) {
+  if (!bytes) return SPA_ERR_NULL;
+  const int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) {
+    *bytes = 0;
+    return SPA_OK;
+  }
+  if (st) return st;
+  *bytes = make_layout(B, H, N, m, dtype).total;
+  return SPA_OK;
+}
+
+int spa_attention_fwd_ws(const void* q, const void* k, const void* v, const void* P, float* out,
+                         int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if ((st = check_forward_ptrs(q, k, v, P, out))) return st;
+  if (!workspace) return SPA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SPA_ERR_ALIGN;
+  if (workspace_bytes < make_layout(B, H, N, m, dtype).total) return SPA_ERR_NOMEM;
+  return run_forward(q, k, v, P, out, B, H, N, d, m, d_v, causal, dtype, workspace,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int spa_attention_fwd(const void* q, const void* k, const void* v, const void* P, float* out,
+                      int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                      void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if ((st = check_forward_ptrs(q, k, v, P, out))) return st;
+  const size_t bytes = make_layout(B, H, N, m, dtype).total;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = run_forward(q, k, v, P, out, B, H, N, d, m, d_v, causal, dtype, ws, s);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st) return st;
+  return cuda_status(fe);
+}
+
+int spa_attention_fwd_host(const void* q, const void* k, const void* v, const void* P,
+                           float* out, int B, int H, int N, int d, int m, int d_v, int causal,
+                           int dtype, void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if (!q || !k || !v || !P || !out) return SPA_ERR_NULL;
+  const size_t es = dtype == SPA_BF16 ? 2 : 4;
+  const size_t BHN = static_cast<size_t>(B) * H * N;
+  const size_t nq = BHN * d * es, nv = BHN * d_v * es, np = static_cast<size_t>(H) * d * m * es;
+  const size_t no = BHN * d_v * sizeof(float);
+  const size_t oq = 0, ok = align256(oq + nq), ov = align256(ok + nq), op = align256(ov + nv),
+               oo = align256(op + np), ow = align256(oo + no);
+  const size_t total = ow + make_layout(B, H, N, m, dtype).total;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* dbuf = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&dbuf), total, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  cudaError_t e = cudaMemcpyAsync(dbuf + oq, q, nq, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + ok, k, nq, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + ov, v, nv, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + op, P, np, cudaMemcpyHostToDevice, s);
+  st = cuda_status(e);
+  if (!st)
+    st = run_forward(dbuf + oq, dbuf + ok, dbuf + ov, dbuf + op, reinterpret_cast<float*>(dbuf + oo),
+                     B, H, N, d, m, d_v, causal, dtype, dbuf + ow, s);
+  if (!st) st = cuda_status(cudaMemcpyAsync(out, dbuf + oo, no, cudaMemcpyDeviceToHost, s));
+  const cudaError_t fe = cudaFreeAsync(dbuf, s);
+  const cudaError_t se = cudaStreamSynchronize(s);
+  if (st) return st;
+  if (fe != cudaSuccess || se != cudaSuccess) return SPA_ERR_CUDA;
+  return SPA_OK;
+}
+
+int spa_device_error(int* code) {
+  if (!code) return SPA_ERR_NULL;
+  int* p = nullptr;
+  int st = device_error_ptr(&p);
+  if (st) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SPA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return SPA_ERR_CUDA;
+  *code = v ? SPA_ERR_TIMEOUT : SPA_OK;
+  return SPA_OK;
+}
+
+}  // extern "C"

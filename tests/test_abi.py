@@ -1,0 +1,138 @@
+"""The C ABI boundary, on the host: the library loads, exports every function
+include/spa.h declares, and rejects bad arguments with the documented status
+codes before touching the GPU (no kernel runs in these tests)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT, spa
+
+HEADER = os.path.join(ROOT, "include", "spa.h")
+
+OK, NULL, SHAPE, DTYPE, ALIGN, UNSUPPORTED, NOMEM = 0, 1, 2, 3, 4, 5, 6
+F32, BF16 = 0, 1
+A = 0x100000  # a 16-byte-aligned dummy address; never dereferenced by validation
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return spa().lib
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("spa_project", "spa_attention_fwd", "spa_status_str"):
+        assert required in names
+
+
+def test_every_declared_function_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported by libspa.so"
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert spa().status_str(code).startswith("SPA_")
+    assert spa().status_str(12345) == "SPA_ERR_UNKNOWN"
+    assert lib.spa_version() >= 100
+
+
+def fwd(lib, q=A, k=A, v=A, P=A, out=A, B=1, H=2, N=256, d=128, m=32, dv=128, causal=0,
+        dtype=BF16):
+    return lib.spa_attention_fwd(q, k, v, P, out, B, H, N, d, m, dv, causal, dtype, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert fwd(lib, q=None) == NULL
+    assert fwd(lib, out=None) == NULL
+    assert fwd(lib, P=None) == NULL
+    assert fwd(lib, N=-1) == SHAPE
+    assert fwd(lib, B=-2) == SHAPE
+    assert fwd(lib, dtype=7) == DTYPE
+    assert fwd(lib, k=A + 8) == ALIGN
+    assert fwd(lib, out=A + 4) == ALIGN
+    assert fwd(lib, B=300, H=300) == SHAPE            # B*H above 65535
+    assert fwd(lib, d=0) == UNSUPPORTED
+    assert fwd(lib, d=257) == UNSUPPORTED
+    assert fwd(lib, m=129) == UNSUPPORTED
+    # bf16 tensor-core path: m in {16,32,64,128}, d_v in {64,128}
+    assert fwd(lib, m=24) == UNSUPPORTED
+    assert fwd(lib, dv=96) == UNSUPPORTED
+    # fp32 path accepts any m <= 128 and d_v <= 256 (still validated before any launch)
+    assert fwd(lib, m=24, dv=96, dtype=F32, q=None) == NULL
+
+
+def test_empty_problem_is_a_no_op(lib):
+    # nothing is read or written, so even NULL pointers are fine
+    assert fwd(lib, q=None, k=None, v=None, P=None, out=None, N=0) == OK
+    assert fwd(lib, q=None, k=None, v=None, P=None, out=None, B=0) == OK
+    assert lib.spa_project(None, None, None, 1, 1, 0, 64, 16, BF16, None) == OK
+
+
+def test_project_rejects_bad_arguments(lib):
+    assert lib.spa_project(None, A, A, 1, 1, 8, 64, 16, BF16, None) == NULL
+    assert lib.spa_project(A, A, A + 2, 1, 1, 8, 64, 16, BF16, None) == ALIGN
+    assert lib.spa_project(A, A, A, 1, 1, 8, 300, 16, BF16, None) == UNSUPPORTED
+    assert lib.spa_project(A, A, A, 1, 1, 8, 64, 16, 9, None) == DTYPE
+
+
+def ws_size(lib, B, H, N, d, m, dv, dtype):
+    n = ctypes.c_size_t(0)
+    st = lib.spa_attention_workspace_size(B, H, N, d, m, dv, dtype, ctypes.byref(n))
+    return st, n.value
+
+
+def _r(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("m,KD", [(16, 48), (32, 32), (64, 64), (128, 128)])
+def test_workspace_size_bf16(lib, m, KD):
+    B, H, N = 1, 32, 32768 + 5
+    NT = (N + 127) // 128
+    tiles = B * H * NT * 128 * KD * 2
+    expect = _r(_r(_r(tiles) + tiles) + B * H * NT * 128 * 4) + _r(B * H * NT * 4)
+    st, n = ws_size(lib, B, H, N, 128, m, 128, BF16)
+    assert st == OK and n == expect
+
+
+def test_workspace_size_f32_and_empty(lib):
+    st, n = ws_size(lib, 1, 1, 256, 64, 16, 64, F32)
+    assert st == OK and n == 2 * _r(256 * 16 * 4)
+    assert ws_size(lib, 1, 1, 0, 64, 16, 64, F32) == (OK, 0)
+    assert ws_size(lib, 1, 1, 8, 64, 24, 64, BF16)[0] == UNSUPPORTED
+    assert lib.spa_attention_workspace_size(1, 1, 8, 64, 16, 64, F32, None) == NULL
+
+
+def test_workspace_entry_point_checks_its_buffer(lib):
+    st, need = ws_size(lib, 1, 2, 256, 128, 32, 128, BF16)
+    args = (A, A, A, A, A, 1, 2, 256, 128, 32, 128, 0, BF16)
+    assert lib.spa_attention_fwd_ws(*args, None, need, None) == NULL
+    assert lib.spa_attention_fwd_ws(*args, A + 16, need, None) == ALIGN
+    assert lib.spa_attention_fwd_ws(*args, A, need - 1, None) == NOMEM
+
+
+def test_host_entry_point_validates_first(lib):
+    assert lib.spa_attention_fwd_host(None, A, A, A, A, 1, 1, 8, 64, 16, 64, 0, BF16, None) == NULL
+    assert lib.spa_attention_fwd_host(A, A, A, A, A, 1, 1, 8, 64, 20, 64, 0, BF16, None) == \
+        UNSUPPORTED
+    assert lib.spa_device_error(None) == NULL
+
+
+def test_binding_marshals_shapes():
+    import torch
+    pkg = spa()
+    q = torch.zeros((1, 2, 8, 16), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkg.spa_attention_fwd(q, q, q, torch.zeros((3, 16, 16), dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        pkg.spa_attention_fwd(q, q, q.float(), torch.zeros((2, 16, 16), dtype=torch.bfloat16))
