@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Throughput of the projected-feature attention forward on GB300.
+
+One step = the whole forward (projection of Q and K, scores, online softmax,
+value product) over one batch of the workload
+    C4: B=1, H=32, N=32768, d=128, m=32, d_v=128, bf16, non-causal,
+        Q, K, V iid N(0, 1), P iid N(0, 1/m) per head
+with inputs resident in HBM.  The metric is TFLOP/s with
+    FLOPs = 4 B H N d m + 2 B H N^2 (m + d_v)     (N^2 term halved if causal)
+and its fraction of the measured bf16 tensor-core peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent problems, no data-path collective: weak scaling); rank 0 prints
+one JSON line.  --impl reference times the fp64 CPU oracle on a bounded sample
+of the same workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "projected-attention fwd TFLOP/s and % of GB300 bf16 tensor peak vs N, m"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ FLOP model
+def proj_flops(B, H, N, d, m) -> float:
+    """Projection of Q and K: 2 GEMMs of (B H N) x d x m."""
+    return 4.0 * B * H * N * d * m
+
+
+def attn_flops(B, H, N, m, dv, causal) -> float:
+    """Scores (2 N^2 m) and value product (2 N^2 d_v) per head, halved when causal."""
+    f = 2.0 * B * H * float(N) * N * (m + dv)
+    return f / 2 if causal else f
+
+
+def flops(B, H, N, d, m, dv, causal) -> float:
+    return proj_flops(B, H, N, d, m) + attn_flops(B, H, N, m, dv, causal)
+
+
+def speedup_vs_standard(d, m, dv, N=None) -> float:
+    """Cost ratio standard / projected attention at the same N (N -> inf if None)."""
+    if N is None:
+        return (d + dv) / (m + dv)
+    std = 2.0 * N * N * (d + dv)
+    return std / (proj_flops(1, 1, N, d, m) + attn_flops(1, 1, N, m, dv, False))
+
+
+# ------------------------------------------------------------------ peaks / counters
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("projected_feature_efficient_gb300/csrc/attn_tc.cu",
+                "projected_feature_efficient_gb300/csrc/ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}_dram.md")
+    try:
+        vals = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    vals[k.strip()] = v.strip().strip("`")
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(vals["dram_bytes_per_full_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: str):
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", device_index],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = [s for t, s in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
+        if not rows:  # the timed region was shorter than one sampling period
+            rows = [s for _, s in self.samples[-3:]]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def physical_device(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+def oracle_sample(w, q, k, v, P, target_s: float):
+    """Time the fp64 oracle on head 0 of the workload, with as many query rows as
+    fit in about target_s seconds.  Returns (flops, seconds, rows, threads)."""
+    import numpy as np
+
+    import oracle
+    q0, k0, v0 = (t[:1, :1].contiguous() for t in (q, k, v))
+    P0 = P[:1].contiguous()
+
+    def run(rows):
+        idx = np.linspace(0, w.N - 1, rows).round().astype(np.int64)
+        t = time.perf_counter()
+        oracle.attention(q0, k0, v0, P0, causal=w.causal, rows=idx)
+        dt = time.perf_counter() - t
+        keys = (idx + 1).sum() if w.causal else rows * w.N
+        fl = 2.0 * w.N * w.d * w.m + 2.0 * rows * w.d * w.m + 2.0 * float(keys) * (w.m + w.dv)
+        return fl, dt
+
+    _, t1 = run(1)
+    _, t64 = run(64)
+    per_row = max((t64 - t1) / 63.0, 1e-6)
+    rows = int(max(1, min(w.N, (target_s - t1) / per_row)))
+    fl, dt = run(rows)
+    return fl, dt, rows, oracle.num_threads()
+
+
+# ------------------------------------------------------------------ arms
+def workload():
+    import spa_inputs as si
+    return si.WORKLOADS["C4"].with_m(32)
+
+
+def config_of(w, world):
+    return {
+        "workload": f"C4: B={w.B} H={w.H} N={w.N} d={w.d} m={w.m} d_v={w.dv} bf16 "
+                    f"{'causal' if w.causal else 'non-causal'}; Q,K,V iid N(0,1); "
+                    f"P iid N(0,1/m) per head",
+        "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "d_v": w.dv, "causal": w.causal,
+        "l2": "inputs (805 MB) larger than L2 (129 MB); no flush between steps",
+        "api": "spa_attention_prepare + spa_attention_apply on a preallocated workspace",
+        "parallelism": f"dp{world} (one independent copy of the workload per GPU)",
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import spa_inputs as si
+    w = workload()
+    q, k, v = si.make_qkv(w)
+    P = si.make_P(w)
+    per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    import numpy as np
+
+    import oracle
+    q0, k0, v0 = (t[:1, :1].contiguous() for t in (q, k, v))
+    P0 = P[:1].contiguous()
+    # size one step: rows of head 0 that take about per_step seconds
+    fl_cal, t_cal, rows, threads = oracle_sample(w, q, k, v, P, per_step)
+    idx = np.linspace(0, w.N - 1, rows).round().astype(np.int64)
+    fl_step = 2.0 * w.N * w.d * w.m + 2.0 * rows * w.d * w.m + 2.0 * rows * w.N * (w.m + w.dv)
+    for _ in range(args.warmup):
+        oracle.attention(q0, k0, v0, P0, causal=w.causal, rows=idx)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(q0, k0, v0, P0, causal=w.causal, rows=idx)
+    dt = time.perf_counter() - t
+    value = fl_step * args.steps / dt / 1e12
+    sample = (f"head 0 of {w.H}, {rows} of {w.N} query rows (evenly spaced) per step, "
+              f"full key range; projection of all {w.N} keys of the head included")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import projected_feature_efficient_gb300 as spa
+    import spa_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload()
+    q_h, k_h, v_h = si.make_qkv(w)
+    P_h = si.make_P(w)
+    q, k, v, P = (t.to(dev) for t in (q_h, k_h, v_h, P_h))
+    B, H, N, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
+    ws = torch.empty(spa.spa_attention_workspace_size(B, H, N, d, m, dv, spa.SPA_BF16),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        spa.spa_attention_prepare(q, k, P, dv, ws)
+        spa.spa_attention_apply(v, ws, B, H, N, d, m, causal=w.causal, out=out)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed_region(sampler):
+        K = args.steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 1)]
+        barrier()
+        sampler.mark_start()
+        ev[0].record(stream)
+        for i in range(K):
+            spa.spa_attention_prepare(q, k, P, dv, ws)
+            ev[2 * i + 1].record(stream)
+            spa.spa_attention_apply(v, ws, B, H, N, d, m, causal=w.causal, out=out)
+            ev[2 * i + 2].record(stream)
+        barrier()
+        sampler.mark_end()
+        total = ev[0].elapsed_time(ev[2 * K])
+        attn = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(K))
+        proj = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(K))
+        return total, attn, proj
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if spa.device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait during warm-up")
+
+    sampler = ClockSampler(physical_device(local_rank))
+    time.sleep(0.3)
+    total, attn, proj = timed_region(sampler)
+    clocks = sampler.summary()
+    remeasured = False
+    if clocks and BAD_REASONS & set(clocks["reasons"]):
+        sampler.stop()
+        sampler = ClockSampler(physical_device(local_rank))
+        time.sleep(0.3)
+        total, attn, proj = timed_region(sampler)
+        clocks = sampler.summary()
+        remeasured = True
+    sampler.stop()
+
+    t = torch.tensor([total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max_ms = float(t.item())
+    K = args.steps
+    f_step = flops(B, H, N, d, m, dv, w.causal)
+    value = world * f_step * K / (t_max_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public host-buffer entry point
+    qp, kp, vp, Pp = (x.pin_memory() for x in (q_h, k_h, v_h, P_h))
+    out_h = torch.empty((B, H, N, dv), dtype=torch.float32).pin_memory()
+    spa.spa_attention_fwd_host(qp, kp, vp, Pp, causal=w.causal, out=out_h)
+    Ke = max(1, min(K, 10))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        spa.spa_attention_fwd_host(qp, kp, vp, Pp, causal=w.causal, out=out_h)
+    te = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = world * f_step * Ke / float(te.item()) / 1e12
+    h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, Pp))
+    d2h = out_h.numel() * out_h.element_size()
+    if spa.device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
+
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        fl, dt, rows, threads = oracle_sample(w, q_h, k_h, v_h, P_h, args.cpu_seconds)
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"head 0 of {w.H}, {rows} of {w.N} query rows (evenly spaced), full "
+                         f"key range, projection of all keys of the head; {dt:.1f} s"}
+
+    if rank == 0:
+        peak, peak_sus, peak_src = load_peaks()
+        attn_ms = attn / K
+        achieved = attn_flops(B, H, N, m, dv, w.causal) / (attn_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": t_max_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, world),
+            "pct_of_peak": 100.0 * value / world / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic("C4_m32"),
+                         "kernel": "attn_tc_kernel (scores + softmax + PV)",
+                         "peak_source": f"{peak_src} bf16 burst",
+                         "frac_of_sustained": achieved / peak_sus},
+            "kernels_ms_per_step": {"projection": proj / K, "attention": attn_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "api": "spa_attention_fwd_host",
+                    "steps": Ke},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+        }
+        if remeasured:
+            line["remeasured_after_throttle"] = True
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -110,6 +110,24 @@ int spa_attention_fwd_ws(const void *q, const void *k, const void *v, const void
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spa_attention_prepare / spa_attention_apply -- the forward in two stages on
+ * a caller-provided workspace (as for spa_attention_fwd_ws).  prepare runs the
+ * projection of q and k and leaves the score operands in the workspace; apply
+ * runs scores, mask, online softmax and the value product from it.  The pair,
+ * called in order on one stream with the same sizes, computes exactly what
+ * spa_attention_fwd_ws computes.  apply may be repeated (other v, other
+ * causal) on one prepared workspace as long as q, k, P and the sizes are
+ * unchanged.  d_v must be passed to prepare as well: it takes part in the
+ * size checks.
+ */
+int spa_attention_prepare(const void *q, const void *k, const void *P, int B, int H, int N,
+                          int d, int m, int d_v, int dtype, void *workspace,
+                          size_t workspace_bytes, void *stream);
+int spa_attention_apply(const void *v, float *out, int B, int H, int N, int d, int m, int d_v,
+                        int causal, int dtype, const void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
  * spa_attention_fwd_host -- end-to-end form on HOST buffers: copies q, k, v, P
  * to the device, runs the forward, copies out back, and synchronises `stream`
  * before returning, so `out` is valid on return.  Device buffers and the

@@ -13,7 +13,8 @@ import importlib
 __all__ = [
     "SPA_BF16", "SPA_F32", "SpaError", "device_error", "lib", "lib_path",
     "spa_attention_fwd", "spa_attention_fwd_host", "spa_attention_fwd_ws",
-    "spa_attention_workspace_size", "spa_project", "status_str",
+    "spa_attention_workspace_size", "spa_attention_prepare", "spa_attention_apply",
+    "spa_project", "status_str",
 ]
 
 

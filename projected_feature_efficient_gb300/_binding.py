@@ -35,6 +35,10 @@ lib.spa_attention_fwd_ws.argtypes = [_vp] * 5 + [_i] * 8 + [_vp, _sz, _vp]
 lib.spa_attention_fwd_ws.restype = _i
 lib.spa_attention_fwd_host.argtypes = [_vp] * 5 + [_i] * 8 + [_vp]
 lib.spa_attention_fwd_host.restype = _i
+lib.spa_attention_prepare.argtypes = [_vp] * 3 + [_i] * 7 + [_vp, _sz, _vp]
+lib.spa_attention_prepare.restype = _i
+lib.spa_attention_apply.argtypes = [_vp] * 2 + [_i] * 8 + [_vp, _sz, _vp]
+lib.spa_attention_apply.restype = _i
 lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
 
@@ -131,6 +135,33 @@ def spa_attention_fwd_ws(q, k, v, P, workspace, causal=False, out=None, stream=N
                                     dv, int(bool(causal)), _dtype_code(q), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(),
                                     _stream_ptr(stream)), "spa_attention_fwd_ws")
+    return out
+
+
+def spa_attention_prepare(q, k, P, dv, workspace, stream=None):
+    """Stage 1 of the forward: project q and k into `workspace` (uint8 device tensor)."""
+    B, H, N, d = q.shape
+    m = P.shape[-1]
+    if tuple(k.shape) != (B, H, N, d) or tuple(P.shape) != (H, d, m):
+        raise ValueError("shapes: q,k [B,H,N,d]; P [H,d,m]")
+    _check(lib.spa_attention_prepare(_ptr(q), _ptr(k), _ptr(P), B, H, N, d, m, dv,
+                                     _dtype_code(q), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_ptr(stream)), "spa_attention_prepare")
+
+
+def spa_attention_apply(v, workspace, B, H, N, d, m, causal=False, out=None, stream=None,
+                        dtype_code=None):
+    """Stage 2 of the forward from a prepared workspace; returns fp32 [B,H,N,dv]."""
+    import torch
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=v.device)
+    code = _dtype_code(v) if dtype_code is None else dtype_code
+    _check(lib.spa_attention_apply(_ptr(v), _ptr(out), B, H, N, d, m, dv, int(bool(causal)),
+                                   code, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream_ptr(stream)), "spa_attention_apply")
     return out
 
 

@@ -105,31 +105,51 @@ Layout make_layout(int B, int H, int N, int m, int dtype) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPA_OK : SPA_ERR_CUDA; }
 
-int run_forward(const void* q, const void* k, const void* v, const void* P, float* out, int B,
-                int H, int N, int d, int m, int dv, int causal, int dtype, void* ws,
-                cudaStream_t stream) {
-  const Layout L = make_layout(B, H, N, m, dtype);
-  const int BH = B * H;
-  char* w = static_cast<char*>(ws);
+spa::ProjParams proj_params(const void* q, const void* k, const void* P, int B, int H, int N,
+                            int d, int m, int dtype, const Layout& L, char* w) {
   spa::ProjParams pp{};
   pp.x[0] = q;
   pp.x[1] = k;
   pp.P = P;
   pp.nx = 2;
-  pp.BH = BH;
+  pp.BH = B * H;
   pp.H = H;
   pp.N = N;
   pp.d = d;
   pp.m = m;
   pp.bf16_in = dtype == SPA_BF16;
-
+  pp.NT = (N + spa::kTileRows - 1) / spa::kTileRows;
   if (dtype == SPA_F32) {
     pp.mode = ProjOut::F32;
     pp.out[0] = w + L.qp;
     pp.out[1] = w + L.kp;
-    pp.NT = (N + spa::kTileRows - 1) / spa::kTileRows;
-    int st = cuda_status(spa::launch_project(pp, stream));
-    if (st) return st;
+  } else {
+    pp.mode = L.mode;
+    pp.out[0] = w + L.qs;
+    pp.out[1] = w + L.ks;
+    pp.mul[0] = reinterpret_cast<float*>(w + L.qmul);
+    pp.mul[1] = reinterpret_cast<float*>(w + L.kmul);
+    // scores come out in base-2 logits: fold log2(e) / sqrt(m) into Q
+    pp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m)));
+  }
+  return pp;
+}
+
+// Stage 1: projection of q and k into the workspace.
+int run_prepare(const void* q, const void* k, const void* P, int B, int H, int N, int d, int m,
+                int dtype, void* ws, cudaStream_t stream) {
+  const Layout L = make_layout(B, H, N, m, dtype);
+  const spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, dtype, L, static_cast<char*>(ws));
+  return cuda_status(spa::launch_project(pp, stream));
+}
+
+// Stage 2: scores, mask, online softmax and the value product from a prepared workspace.
+int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int causal,
+              int dtype, const void* ws, cudaStream_t stream) {
+  const Layout L = make_layout(B, H, N, m, dtype);
+  const int BH = B * H;
+  const char* w = static_cast<const char*>(ws);
+  if (dtype == SPA_F32) {
     spa::AttnF32Params ap{};
     ap.Qp = reinterpret_cast<const float*>(w + L.qp);
     ap.Kp = reinterpret_cast<const float*>(w + L.kp);
@@ -143,18 +163,7 @@ int run_forward(const void* q, const void* k, const void* v, const void* P, floa
     ap.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
     return cuda_status(spa::launch_attn_f32(ap, stream));
   }
-
-  pp.mode = L.mode;
-  pp.NT = L.NT;
-  pp.out[0] = w + L.qs;
-  pp.out[1] = w + L.ks;
-  pp.mul[0] = reinterpret_cast<float*>(w + L.qmul);
-  pp.mul[1] = reinterpret_cast<float*>(w + L.kmul);
-  // scores come out in base-2 logits: fold log2(e) / sqrt(m) into Q
-  pp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m)));
-  int st = cuda_status(spa::launch_project(pp, stream));
-  if (st) return st;
-
+  int st;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   if ((st = get_encode(&encode))) return st;
   spa::AttnTcParams ap{};
@@ -184,6 +193,14 @@ int run_forward(const void* q, const void* k, const void* v, const void* P, floa
   ap.causal = causal != 0;
   ap.f16_ops = L.mode == ProjOut::F16X1;
   return cuda_status(spa::launch_attn_tc(ap, stream));
+}
+
+int run_forward(const void* q, const void* k, const void* v, const void* P, float* out, int B,
+                int H, int N, int d, int m, int dv, int causal, int dtype, void* ws,
+                cudaStream_t stream) {
+  int st = run_prepare(q, k, P, B, H, N, d, m, dtype, ws, stream);
+  if (st) return st;
+  return run_apply(v, out, B, H, N, m, dv, causal, dtype, ws, stream);
 }
 
 int check_forward_ptrs(const void* q, const void* k, const void* v, const void* P,
@@ -265,6 +282,34 @@ int spa_attention_fwd_ws(const void* q, const void* k, const void* v, const void
   if (workspace_bytes < make_layout(B, H, N, m, dtype).total) return SPA_ERR_NOMEM;
   return run_forward(q, k, v, P, out, B, H, N, d, m, d_v, causal, dtype, workspace,
                      static_cast<cudaStream_t>(stream));
+}
+
+int spa_attention_prepare(const void* q, const void* k, const void* P, int B, int H, int N,
+                          int d, int m, int d_v, int dtype, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if (!q || !k || !P || !workspace) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(P) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SPA_ERR_ALIGN;
+  if (workspace_bytes < make_layout(B, H, N, m, dtype).total) return SPA_ERR_NOMEM;
+  return run_prepare(q, k, P, B, H, N, d, m, dtype, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int spa_attention_apply(const void* v, float* out, int B, int H, int N, int d, int m, int d_v,
+                        int causal, int dtype, const void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if (!v || !out || !workspace) return SPA_ERR_NULL;
+  if (!aligned16(v) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SPA_ERR_ALIGN;
+  if (workspace_bytes < make_layout(B, H, N, m, dtype).total) return SPA_ERR_NOMEM;
+  return run_apply(v, out, B, H, N, m, d_v, causal, dtype, workspace,
+                   static_cast<cudaStream_t>(stream));
 }
 
 int spa_attention_fwd(const void* q, const void* k, const void* v, const void* P, float* out,
