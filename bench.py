@@ -62,6 +62,25 @@ def speedup_vs_standard(d, m, dv, N=None) -> float:
     return std / (proj_flops(1, 1, N, d, m) + attn_flops(1, 1, N, m, dv, False))
 
 
+# ------------------------------------------------------------------ multi-GPU host logic
+def shard_range(total: int, world: int, rank: int):
+    """Contiguous share [lo, hi) of `total` independent units (batch entries or
+    (b, h) pairs) owned by `rank`; shares differ in size by at most one."""
+    base, extra = divmod(total, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest of every rank's value (identity on one process)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ peaks / counters
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -275,7 +294,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = workload()
-    q_h, k_h, v_h = si.make_qkv(w)
+    lo, _ = shard_range(world * w.B, world, rank)
+    q_h, k_h, v_h = si.make_qkv(w, seed=None if lo == 0 else 1000 + w.number + 7919 * lo)
     P_h = si.make_P(w)
     q, k, v, P = (t.to(dev) for t in (q_h, k_h, v_h, P_h))
     B, H, N, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
@@ -331,10 +351,7 @@ def run_ours(args, rank, world, local_rank):
         remeasured = True
     sampler.stop()
 
-    t = torch.tensor([total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    t_max_ms = float(t.item())
+    t_max_ms = max_over_ranks(total, dist, dev)
     K = args.steps
     f_step = flops(B, H, N, d, m, dv, w.causal)
     value = world * f_step * K / (t_max_ms * 1e-3) / 1e12
@@ -348,10 +365,8 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.perf_counter()
     for _ in range(Ke):
         spa.spa_attention_fwd_host(qp, kp, vp, Pp, causal=w.causal, out=out_h)
-    te = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * f_step * Ke / float(te.item()) / 1e12
+    te = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    e2e_value = world * f_step * Ke / te / 1e12
     h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, Pp))
     d2h = out_h.numel() * out_h.element_size()
     if spa.device_error() != 0:
