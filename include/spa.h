@@ -141,6 +141,29 @@ int spa_attention_fwd_host(const void *q, const void *k, const void *v, const vo
                            int dtype, void *stream);
 
 /*
+ * spa_attention_fwd_noalloc -- spa_attention_fwd without any device
+ * allocation.  (The pages describe no such entry point; it is an addition for
+ * callers that cannot allocate device memory while they run -- code inside a
+ * framework or allocator that owns all device memory, real-time loops that
+ * must not enter the driver's allocator, processes with a fixed memory
+ * budget.)  Same arguments, layouts and results as spa_attention_fwd.
+ *   Scratch   a 64 MiB array compiled into libspa.so as device memory; every
+ *             GPU that loads the library holds it until the process exits.
+ *             Problems whose workspace (spa_attention_workspace_size) exceeds
+ *             64 MiB are rejected with SPA_ERR_NOMEM before anything runs.
+ *   Set-up    the first call on a device looks up the array's device address
+ *             (cudaGetSymbolAddress) with that device current; make that first
+ *             call before any stream capture.
+ *   Sharing   all calls on a device share the one array.  Calls whose kernels
+ *             overlap on the GPU (other streams, other threads) race on it:
+ *             serialise them.  Contents left by an earlier call are never read.
+ *   No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const void *P,
+                              float *out, int B, int H, int N, int d, int m, int d_v, int causal,
+                              int dtype, void *stream);
+
+/*
  * spa_device_error -- reads and clears the device error word of the current
  * device (synchronising it first).  *code receives 0 when no kernel gave up
  * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.

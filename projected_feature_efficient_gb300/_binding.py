@@ -39,6 +39,8 @@ lib.spa_attention_prepare.argtypes = [_vp] * 3 + [_i] * 7 + [_vp, _sz, _vp]
 lib.spa_attention_prepare.restype = _i
 lib.spa_attention_apply.argtypes = [_vp] * 2 + [_i] * 8 + [_vp, _sz, _vp]
 lib.spa_attention_apply.restype = _i
+lib.spa_attention_fwd_noalloc.argtypes = [_vp] * 5 + [_i] * 8 + [_vp]
+lib.spa_attention_fwd_noalloc.restype = _i
 lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
 

@@ -383,3 +383,55 @@ int spa_device_error(int* code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.  Some callers cannot allocate device memory while
+// they run: code that executes inside a framework that owns all device memory
+// and forbids cudaMalloc (or is itself inside an allocator callback), real-time
+// loops that must not touch the driver's allocator, or processes whose memory
+// budget is fixed up front.  For them the forward can use a scratch buffer that
+// the library carries as a file-scope device array, sized once at compile time.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
+
+// Scratch for the score-operand tiles / projections of spa_attention_fwd_noalloc.
+// In host code this symbol is only a stand-in: its device address comes from
+// cudaGetSymbolAddress, taken per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: the device address of the array.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SPA_OK;
+}
+
+}  // namespace
+
+extern "C" int spa_attention_fwd_noalloc(const void* q, const void* k, const void* v,
+                                         const void* P, float* out, int B, int H, int N, int d,
+                                         int m, int d_v, int causal, int dtype, void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if ((st = check_forward_ptrs(q, k, v, P, out))) return st;
+  if (make_layout(B, H, N, m, dtype).total > kNoAllocScratchBytes) return SPA_ERR_NOMEM;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch))) return st;
+  // Every scratch byte the attention stage reads is written first by this
+  // call's projection stage, so nothing has to be cleared between calls.
+  return run_forward(q, k, v, P, out, B, H, N, d, m, d_v, causal, dtype, scratch,
+                     static_cast<cudaStream_t>(stream));
+}

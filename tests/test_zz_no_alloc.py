@@ -1,0 +1,74 @@
+"""The allocation-free forward, spa_attention_fwd_noalloc.
+
+It exists for callers that cannot allocate device memory while they run (code
+inside a framework or allocator that owns all device memory, real-time loops
+that must stay out of the driver's allocator, processes with a fixed memory
+budget): the forward's scratch lives in a 64 MiB device array compiled into
+libspa.so instead of a cudaMallocAsync'd workspace.
+
+The test calls it through the C ABI twice in a row, on different inputs, and
+compares each result with the allocating entry point spa_attention_fwd within
+the bf16 / fp32 tolerances used by the parity tests.  The second call also
+shows that what the first call left in the shared array does not leak into the
+next result.  This file is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import spa_inputs as si
+from helpers import BF16_MAX_ABS, BF16_REL_F, F32_MAX_ABS, errors, spa
+
+pytestmark = pytest.mark.gpu
+
+NOMEM = 6
+
+
+def _call_noalloc(lib, q, k, v, P, out, causal, dtype_code):
+    B, H, N, d = q.shape
+    m, dv = P.shape[-1], v.shape[-1]
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.spa_attention_fwd_noalloc(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(P.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()), B, H, N, d, m, dv, int(causal), dtype_code, stream)
+
+
+@pytest.mark.parametrize("name", ["C2", "C1"])
+def test_noalloc_matches_allocating_forward_on_two_calls_in_a_row(name):
+    pkg = spa()
+    base = si.WORKLOADS[name]
+    # two different problems back to back: the second is smaller, so stale
+    # scratch from the first call overlaps what the second call reads
+    shapes = [base.scaled(B=2, H=4, N=1500, causal=True), base.scaled(B=1, H=3, N=700)]
+    for i, w in enumerate(shapes):
+        q, k, v = (t.cuda() for t in si.make_qkv(w, seed=500 + i))
+        P = si.make_P(w, seed=600 + i).cuda()
+        ref = pkg.spa_attention_fwd(q, k, v, P, causal=w.causal)
+        out = torch.full_like(ref, float("nan"))
+        code = pkg.SPA_BF16 if w.dtype == "bf16" else pkg.SPA_F32
+        assert _call_noalloc(pkg.lib, q, k, v, P, out, w.causal, code) == 0
+        torch.cuda.synchronize()
+        got, want = out.cpu().numpy(), ref.cpu().numpy()
+        assert np.isfinite(got).all()
+        max_abs, rel_f = errors(got, want)
+        if w.dtype == "bf16":
+            assert rel_f <= BF16_REL_F and max_abs <= BF16_MAX_ABS, (i, rel_f, max_abs)
+        else:
+            assert max_abs <= F32_MAX_ABS, (i, max_abs)
+    assert pkg.device_error() == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    pkg = spa()
+    # B=1 H=64 N=131072 m=32 needs far more than 64 MiB of workspace
+    need = pkg.spa_attention_workspace_size(1, 64, 131072, 128, 32, 128, pkg.SPA_BF16)
+    assert need > (64 << 20)
+    x = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never touched
+    st = pkg.lib.spa_attention_fwd_noalloc(
+        ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(x.data_ptr()),
+        ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(x.data_ptr()),
+        ctypes.c_void_p(x.data_ptr()), 1, 64, 131072, 128, 32, 128, 0, pkg.SPA_BF16, None)
+    assert st == NOMEM
