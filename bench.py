@@ -95,7 +95,7 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("projected_feature_efficient_gb300/csrc/attn_tc.cu",
+    for rel in ("projected_feature_efficient_gb300/csrc/attn_ws.cu",
                 "projected_feature_efficient_gb300/csrc/ptx.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
@@ -105,7 +105,7 @@ def kernel_source_hash() -> str:
 def recorded_traffic(workload: str):
     """DRAM bytes per attention launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}_dram.md")
+    path = os.path.join(ROOT, "profiles", f"attn_ws_{workload}_dram.md")
     try:
         vals = {}
         with open(path) as f:
@@ -225,14 +225,16 @@ def oracle_sample(w, q, k, v, P, target_s: float):
 
 
 # ------------------------------------------------------------------ arms
-def workload():
+def workload(heads=None, m=32):
+    """The C4 workload (optionally with fewer heads, for profiling captures)."""
     import spa_inputs as si
-    return si.WORKLOADS["C4"].with_m(32)
+    w = si.WORKLOADS["C4"].with_m(m)
+    return w.scaled(H=heads) if heads else w
 
 
 def config_of(w, world):
     return {
-        "workload": f"C4: B={w.B} H={w.H} N={w.N} d={w.d} m={w.m} d_v={w.dv} bf16 "
+        "workload": f"C4{'' if w.H == 32 else '-subset'}: B={w.B} H={w.H} N={w.N} d={w.d} m={w.m} d_v={w.dv} bf16 "
                     f"{'causal' if w.causal else 'non-causal'}; Q,K,V iid N(0,1); "
                     f"P iid N(0,1/m) per head",
         "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "d_v": w.dv, "causal": w.causal,
@@ -246,7 +248,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import spa_inputs as si
-    w = workload()
+    w = workload(args.heads, args.m)
     q, k, v = si.make_qkv(w)
     P = si.make_P(w)
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -293,7 +295,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w = workload()
+    w = workload(args.heads, args.m)
     lo, _ = shard_range(world * w.B, world, rank)
     q_h, k_h, v_h = si.make_qkv(w, seed=None if lo == 0 else 1000 + w.number + 7919 * lo)
     P_h = si.make_P(w)
@@ -392,8 +394,8 @@ def run_ours(args, rank, world, local_rank):
             "pct_of_peak": 100.0 * value / world / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": recorded_traffic("C4_m32"),
-                         "kernel": "attn_tc_kernel (scores + softmax + PV)",
+                         "traffic": recorded_traffic(f"C4_m{m}") if w.H == 32 else None,
+                         "kernel": "attn_ws_kernel (scores + softmax + PV)",
                          "peak_source": f"{peak_src} bf16 burst",
                          "frac_of_sustained": achieved / peak_sus},
             "kernels_ms_per_step": {"projection": proj / K, "attention": attn_ms},
@@ -423,6 +425,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run C4 with fewer heads (smaller case for profiler captures)")
+    ap.add_argument("--m", type=int, default=32, choices=(16, 32, 64),
+                    help="projection width of the C4 sweep")
     args = ap.parse_args(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

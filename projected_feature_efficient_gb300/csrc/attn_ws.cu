@@ -1,0 +1,379 @@
+// attn_ws.cu -- warp-specialised fused projected-feature attention on tcgen05
+// (bf16 inputs, fp16 or split-bf16 score operands, fp32 accumulation).
+//
+// One CTA owns two 128-row query tiles (t = 0, 1) of one (batch, head) and
+// streams the key/value tiles of that head once for both.  Ten warps:
+//   warps 0-3  softmax for query tile 0   (TMEM lanes 0-127 of S0 / O0)
+//   warps 4-7  softmax for query tile 1   (TMEM lanes 0-127 of S1 / O1)
+//   warp  8    loads: the two Qp tiles once, then a ring of STAGES Kp tiles
+//              (one bulk copy each) and V tiles (TMA, 128-byte swizzle)
+//   warp  9    tensor-memory allocation and tcgen05.mma issue
+// Tensor memory (512 columns):  S0 | S1 | O0 | O1, with the bf16 probabilities
+// P_t written over the first 64 columns of S_t and read from there by the PV
+// product.  The MMA issue order per key tile j is
+//   PV0(j), S0(j+1), PV1(j), S1(j+1)
+// so while one softmax warpgroup works on its tile, the tensor cores run the
+// other tile's products (ping-pong).  MMAs from one thread execute in issue
+// order, so S_t(j+1) never overwrites P_t(j) before PV_t(j) has read it, and
+// the commit that signals "S_t(j+1) ready" also covers PV_t(j), which lets the
+// softmax rescale O_t right after it without another wait.
+//
+// Online softmax (base 2, log2(e)/sqrt(m) already folded into Qp): the
+// running max only moves when a tile's max exceeds it by more than 8; in
+// between, probabilities up to 2^8 are accumulated, which leaves the final
+// O / l unchanged up to rounding and skips most rescales of O.
+//
+// Every wait is bounded (2 s).  A role that gives up sets the CTA abort flag
+// and the device error word; every role leaves its loop, the MMA issuer and
+// the loader wait (bounded) for their own operations in flight, and TMEM is
+// freed before the CTA exits.
+#include <math.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace spa {
+namespace {
+
+using namespace ptx;
+
+constexpr uint64_t kLimitNs = 2000000000ull;
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return reinterpret_cast<uint8_t*>((a + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+template <int KD, int DV>
+struct WsPlan {
+  static constexpr int kStages = KD >= 128 ? 2 : 3;
+  static constexpr int kQBytes = kTileRows * KD * 2;
+  static constexpr int kKBytes = kTileRows * KD * 2;
+  static constexpr int kVBytes = kTileRows * DV * 2;
+  static constexpr int kQ = 0;                          // two Q tiles
+  static constexpr int kK = 2 * kQBytes;
+  static constexpr int kV = kK + kStages * kKBytes;
+  static constexpr int kBytes = kV + kStages * kVBytes;
+  // one CTA per SM: a second one would wait in tcgen05.alloc for the 512 columns
+  static constexpr int kLaunch = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
+  static constexpr uint32_t kColsS0 = 0, kColsS1 = 128, kColsO0 = 256, kColsO1 = 256 + DV;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_final;
+  uint64_t drain;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int* err) {
+  if (*abort) return false;
+  if (mbar_wait(bar, parity, kLimitNs)) return true;
+  *abort = 1;
+  atomicExch(err, 1);
+  return false;
+}
+
+template <int KD, int DV, bool F16OPS>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_ws_kernel(const AttnTcParams p, const __grid_constant__ CUtensorMap vmap) {
+  using Plan = WsPlan<KD, DV>;
+  constexpr int S = Plan::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1k(smem_raw);
+  __shared__ Bars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NT = p.NT;
+  const int NP = (NT + 1) >> 1;
+  const int bh = blockIdx.x / NP;
+  const int pair = NP - 1 - static_cast<int>(blockIdx.x % NP);  // longest causal work first
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const int nkv0 = p.causal ? qt0 + 1 : NT;
+  const int nkv1 = qt1 < NT ? (p.causal ? qt1 + 1 : NT) : 0;
+  const int nkv = max(nkv0, nkv1);
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bars.q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], 128);
+    }
+    mbar_init(&bars.o_final, 1);
+    mbar_init(&bars.drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base_sh;
+  constexpr int kTileElems = kTileRows * KD;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ loader
+    if (lane == 0) {
+      prefetch_tmap(&vmap);
+      const uint16_t* Qs = p.Qs + (static_cast<size_t>(bh) * NT + qt0) * kTileElems;
+      const uint16_t* Ks = p.Ks + static_cast<size_t>(bh) * NT * kTileElems;
+      mbar_arrive_expect_tx(&bars.q_full, (nkv1 > 0 ? 2 : 1) * Plan::kQBytes);
+      bulk_g2s(smem + Plan::kQ, Qs, Plan::kQBytes, &bars.q_full);
+      if (nkv1 > 0) bulk_g2s(smem + Plan::kQ + Plan::kQBytes, Qs + kTileElems, Plan::kQBytes,
+                             &bars.q_full);
+      int armed_k = 0, armed_v = 0;  // steps whose K / V copies were started
+      for (int j = 0; j < nkv; ++j) {
+        const int slot = j % S;
+        const uint32_t ph = (j / S) & 1;
+        if (j >= S && !wait_or_abort(&bars.k_empty[slot], ph ^ 1, &abort_sh, p.err)) break;
+        mbar_arrive_expect_tx(&bars.k_full[slot], Plan::kKBytes);
+        bulk_g2s(smem + Plan::kK + slot * Plan::kKBytes, Ks + static_cast<size_t>(j) * kTileElems,
+                 Plan::kKBytes, &bars.k_full[slot]);
+        armed_k = j + 1;
+        if (j >= S && !wait_or_abort(&bars.v_empty[slot], ph ^ 1, &abort_sh, p.err)) break;
+        mbar_arrive_expect_tx(&bars.v_full[slot], Plan::kVBytes);
+        uint8_t* vdst = smem + Plan::kV + slot * Plan::kVBytes;
+#pragma unroll
+        for (int h = 0; h < DV / 64; ++h)
+          tma_load_3d(vdst + h * 16384, &vmap, h * 64, j * kTileRows, bh, &bars.v_full[slot]);
+        armed_v = j + 1;
+      }
+      if (abort_sh) {
+        // let every copy this thread started land before the CTA's memory is reused
+        mbar_wait(&bars.q_full, 0, kLimitNs);
+        for (int j = max(0, armed_k - S); j < armed_k; ++j)
+          mbar_wait(&bars.k_full[j % S], (j / S) & 1, kLimitNs);
+        for (int j = max(0, armed_v - S); j < armed_v; ++j)
+          mbar_wait(&bars.v_full[j % S], (j / S) & 1, kLimitNs);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_f16(128, 128, F16OPS ? kFmtF16 : kFmtBF16, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_f16(128, DV, kFmtBF16, 0, 1);
+      const uint32_t sQ0 = smem_u32(smem + Plan::kQ), sQ1 = sQ0 + Plan::kQBytes;
+      const uint32_t sK = smem_u32(smem + Plan::kK), sV = smem_u32(smem + Plan::kV);
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t a = t == 0 ? sQ0 : sQ1;
+        const uint32_t b = sK + slot * Plan::kKBytes;
+        const uint32_t d = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
+#pragma unroll
+        for (int s = 0; s < KD / 16; ++s)
+          mma_ss(d, smem_desc(a + s * 4096, 2048, 128, kLayoutInterleave),
+                 smem_desc(b + s * 4096, 2048, 128, kLayoutInterleave), kIdescS, s > 0);
+        mma_commit(&bars.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t a = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
+        const uint32_t d = tb + (t == 0 ? Plan::kColsO0 : Plan::kColsO1);
+        const uint32_t b = sV + slot * Plan::kVBytes;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ts(d, a + s * 8, smem_desc(b + s * 2048, 16384, 1024, kLayoutSwizzle128), kIdescPV,
+                 (acc || s > 0) ? 1u : 0u);
+      };
+      bool ok = wait_or_abort(&bars.q_full, 0, &abort_sh, p.err) &&
+                wait_or_abort(&bars.k_full[0], 0, &abort_sh, p.err);
+      if (ok) {
+        tc_fence_after();
+        if (nkv0 > 0) issue_s(0, 0);
+        if (nkv1 > 0) issue_s(1, 0);
+        mma_commit(&bars.k_empty[0]);
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int slot = j % S;
+        const uint32_t ph = (j / S) & 1;
+        if (!(ok = wait_or_abort(&bars.v_full[slot], ph, &abort_sh, p.err))) break;
+        if (j < nkv0) {
+          if (!(ok = wait_or_abort(&bars.p_full[0], j & 1, &abort_sh, p.err))) break;
+          tc_fence_after();
+          issue_pv(0, slot, j > 0);
+        }
+        const int jn = j + 1;
+        const int slotn = jn % S;
+        if (jn < nkv) {
+          if (!(ok = wait_or_abort(&bars.k_full[slotn], (jn / S) & 1, &abort_sh, p.err))) break;
+          tc_fence_after();
+          if (jn < nkv0) issue_s(0, slotn);
+        }
+        if (j < nkv1) {
+          if (!(ok = wait_or_abort(&bars.p_full[1], j & 1, &abort_sh, p.err))) break;
+          tc_fence_after();
+          issue_pv(1, slot, j > 0);
+        }
+        mma_commit(&bars.v_empty[slot]);
+        if (jn < nkv) {
+          if (jn < nkv1) issue_s(1, slotn);
+          mma_commit(&bars.k_empty[slotn]);
+        }
+      }
+      mma_commit(ok ? &bars.o_final : &bars.drain);
+      if (!ok) mbar_wait(&bars.drain, 0, kLimitNs);  // own MMAs in flight
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int r = tid & 127;  // row within the tile == TMEM lane
+    const int nkv_t = t == 0 ? nkv0 : nkv1;
+    const int qt = t == 0 ? qt0 : qt1;
+    const int row = qt * kTileRows + r;
+    const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t tS = lane_base + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
+    const uint32_t tO = lane_base + (t == 0 ? Plan::kColsO0 : Plan::kColsO1);
+    const float qm = nkv_t > 0 ? p.qmul[static_cast<size_t>(bh) * NT * kTileRows + row] : 0.f;
+    const float* kmul = p.kmul + static_cast<size_t>(bh) * NT;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv_t; ++j) {
+      const float km = __ldg(kmul + j);
+      if (!(ok = wait_or_abort(&bars.s_full[t], j & 1, &abort_sh, p.err))) break;
+      tc_fence_after();
+      float x[128];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tS + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(v[i]);
+      }
+      // keys of this tile visible to this row
+      int kvalid = 128;
+      if (j == NT - 1) kvalid = p.N - j * kTileRows;
+      if (p.causal && j == qt) kvalid = min(kvalid, r + 1);
+      if (kvalid < 128) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = c < kvalid ? x[c] : -INFINITY;
+      }
+      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, x[c]);
+        mx1 = fmaxf(mx1, x[c + 1]);
+        mx2 = fmaxf(mx2, x[c + 2]);
+        mx3 = fmaxf(mx3, x[c + 3]);
+      }
+      const float mult = qm * km;  // > 0: range exponents times log2(e)/sqrt(m)
+      const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mult;
+      const bool grow = tmax > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_run - tmax);  // 0 on the first tile
+        m_run = tmax;
+      }
+      const float neg_m = -m_run;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = h * 32 + 2 * i;
+          const float e0 = ex2(fmaf(x[c], mult, neg_m));
+          const float e1 = ex2(fmaf(x[c + 1], mult, neg_m));
+          if (i & 1) { s2 += e0; s3 += e1; } else { s0 += e0; s1 += e1; }
+          pk[i] = pack_bf16x2(e0, e1);
+        }
+        tmem_st16(tS + h * 16, pk);
+      }
+      // O row *= alpha when the max moved; PV(j-1) is complete (covered by the
+      // S(j) commit) and PV(j) waits for p_full below.
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tO + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st16(tO + c0, v);
+        }
+      }
+      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[t]);
+    }
+    // epilogue: O / l -> out (fp32)
+    if (ok && nkv_t > 0) {
+      if (wait_or_abort(&bars.o_final, 0, &abort_sh, p.err)) {
+        tc_fence_after();
+        const float inv = 1.f / l_run;
+        float* dst = p.out + (static_cast<size_t>(bh) * p.N + row) * DV;
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tO + c0, v);
+          tmem_wait_ld();
+          if (row < p.N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float4 o4 = make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                                      __uint_as_float(v[i + 2]) * inv,
+                                      __uint_as_float(v[i + 3]) * inv);
+              *reinterpret_cast<float4*>(dst + c0 + i) = o4;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_dealloc(tb, 512);
+}
+
+template <int KD, int DV, bool F16OPS>
+cudaError_t launch_ws(const AttnTcParams& p, cudaStream_t stream) {
+  using Plan = WsPlan<KD, DV>;
+  auto kern = attn_ws_kernel<KD, DV, F16OPS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Plan::kLaunch);
+  if (e != cudaSuccess) return e;
+  const long long blocks = static_cast<long long>((p.NT + 1) / 2) * p.BH;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kThreads, Plan::kLaunch, stream>>>(p, p.vmap);
+  return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_ws_dv(const AttnTcParams& p, cudaStream_t stream) {
+  if (!p.f16_ops) {
+    if (p.KD == 48) return launch_ws<48, DV, false>(p, stream);
+    return cudaErrorInvalidValue;
+  }
+  switch (p.KD) {
+    case 32: return launch_ws<32, DV, true>(p, stream);
+    case 64: return launch_ws<64, DV, true>(p, stream);
+    case 128: return launch_ws<128, DV, true>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_ws(const AttnTcParams& p, cudaStream_t stream) {
+  if (p.dv == 64) return launch_ws_dv<64>(p, stream);
+  if (p.dv == 128) return launch_ws_dv<128>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace spa

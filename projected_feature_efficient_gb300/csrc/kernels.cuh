@@ -46,7 +46,7 @@ struct AttnTcParams {
   int BH, N, NT, KD, dv, causal;
   int f16_ops;           // 1: fp16 score operands, 0: bf16
 };
-cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t stream);
+cudaError_t launch_attn_ws(const AttnTcParams& p, cudaStream_t stream);
 
 struct AttnF32Params {
   const float* Qp;       // [BH][N][m]

@@ -192,7 +192,7 @@ int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int
   ap.dv = dv;
   ap.causal = causal != 0;
   ap.f16_ops = L.mode == ProjOut::F16X1;
-  return cuda_status(spa::launch_attn_tc(ap, stream));
+  return cuda_status(spa::launch_attn_ws(ap, stream));
 }
 
 int run_forward(const void* q, const void* k, const void* v, const void* P, float* out, int B,
