@@ -246,14 +246,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float km = __ldg(kmul + j);
       if (!(ok = wait_or_abort(&bars.s_full[t], j & 1, &abort_sh, p.err))) break;
       tc_fence_after();
+      // the whole S row: four loads in flight, one wait
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      tmem_ld32(tS, v0);
+      tmem_ld32(tS + 32, v1);
+      tmem_ld32(tS + 64, v2);
+      tmem_ld32(tS + 96, v3);
+      tmem_wait_ld();
       float x[128];
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tS + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(v[i]);
+      for (int i = 0; i < 32; ++i) {
+        x[i] = __uint_as_float(v0[i]);
+        x[32 + i] = __uint_as_float(v1[i]);
+        x[64 + i] = __uint_as_float(v2[i]);
+        x[96 + i] = __uint_as_float(v3[i]);
       }
       // keys of this tile visible to this row
       int kvalid = 128;

@@ -32,7 +32,11 @@ struct ProjParams {
   float qscale;          // factor folded into tensor 0 before conversion (tile modes)
   int bf16_in;           // element type of x and P: 1 = bf16, 0 = fp32
   ProjOut mode;
+  int use_tc;            // tile modes: tensor-core kernel if the shape allows it
+  CUtensorMap xmap[2];   // x[0], x[1] as 3-D (d, N, BH), bf16, 128-byte swizzle, box (64,128,1)
+  int* err;              // device error word
 };
+bool project_tc_eligible(const ProjParams& p);
 cudaError_t launch_project(const ProjParams& p, cudaStream_t stream);
 
 struct AttnTcParams {

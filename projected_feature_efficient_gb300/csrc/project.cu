@@ -2,10 +2,16 @@
 // Sec. 3.1.2 and Algorithm 1 steps 2-3; "Projection-Decomposition Attention",
 // Algorithm 2.1 step 1).
 //
-// One CTA of 128 threads owns a tile of 128 rows of one (batch, head); thread r
-// computes row r.  P_h is staged in shared memory as fp32 (bf16 -> fp32 is
-// exact) and read as a broadcast; X is staged 32 columns at a time.  Every
-// product of two inputs is exact in fp32 and the sum is an fp32 FMA chain.
+// Two kernels compute it:
+//   project_tc_kernel  (bf16 inputs, d a multiple of 8, score-operand output):
+//       a 128-row tile of X arrives by TMA (128-byte swizzle, K-major), P_h^T
+//       is written into shared memory in the tensor cores' interleaved layout,
+//       and one tcgen05 GEMM of shape 128 x m x d accumulates Xp in TMEM (fp32).
+//   project_kernel     (any d, fp32 or bf16 inputs, any output mode):
+//       SIMT fp32 FMA; thread r of a 128-thread CTA computes row r with P_h
+//       staged in shared memory.
+// Either way every product of two inputs is exact in fp32 and the sums are
+// fp32.  The projection is HBM-bound (about 25 FLOP per byte at d=128, m=32).
 //
 // Output modes:
 //   F32     plain fp32 rows, [BH][N][m]  (spa_project, and the fp32 path).
@@ -25,6 +31,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace spa {
 namespace {
@@ -50,6 +57,67 @@ __device__ __forceinline__ int range_exponent(float amax) {
   return max(-125, min(125, e));
 }
 
+// Scale, convert and store row `tid` of a score-operand tile, plus its range
+// multiplier.  Called by all 128 threads of the CTA (it may synchronise them).
+template <int MP, ProjOut MODE>
+__device__ __forceinline__ void store_tile(const ProjParams& p, float (&acc)[MP], int tile,
+                                           int bh, int which, int tid, float* red) {
+  constexpr int KD = MODE == ProjOut::BF16X3 ? 3 * MP : MP;
+  const int row = tile * kTileRows + tid;
+  uint16_t* tout = static_cast<uint16_t*>(which == 0 ? p.out[0] : p.out[1]) +
+                   (static_cast<size_t>(bh) * p.NT + tile) * (kTileRows * KD);
+  const float sc = which == 0 ? p.qscale : 1.f;
+#pragma unroll
+  for (int k = 0; k < MP; ++k) acc[k] *= sc;
+
+  uint16_t vals[KD];
+  if constexpr (MODE == ProjOut::F16X1) {
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < MP; ++k) amax = fmaxf(amax, fabsf(acc[k]));
+    if (which == 1) {  // one exponent for the whole K tile
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if ((tid & 31) == 0) red[tid >> 5] = amax;
+      __syncthreads();
+      amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    }
+    const int e = range_exponent(amax);
+    const float down = pow2i(-e);
+#pragma unroll
+    for (int k = 0; k < MP; ++k) vals[k] = f16_bits(acc[k] * down);
+    if (which == 0)
+      p.mul[0][static_cast<size_t>(bh) * p.NT * kTileRows + row] = pow2i(e);
+    else if (tid == 0)
+      p.mul[1][static_cast<size_t>(bh) * p.NT + tile] = pow2i(e);
+  } else {
+#pragma unroll
+    for (int k = 0; k < MP; ++k) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(acc[k]);
+      const uint16_t hib = __bfloat16_as_ushort(hi);
+      const uint16_t lob = bf16_bits(acc[k] - __bfloat162float(hi));
+      vals[k] = hib;                                   // segment 0: hi for both
+      vals[MP + k] = which == 0 ? hib : lob;           // Q: hi, K: lo
+      vals[2 * MP + k] = which == 0 ? lob : hib;       // Q: lo, K: hi
+    }
+    if (which == 0)
+      p.mul[0][static_cast<size_t>(bh) * p.NT * kTileRows + row] = 1.f;
+    else if (tid == 0)
+      p.mul[1][static_cast<size_t>(bh) * p.NT + tile] = 1.f;
+  }
+  // interleaved core-matrix layout: 8 columns (16 bytes) per store
+#pragma unroll
+  for (int c8 = 0; c8 < KD / 8; ++c8) {
+    uint4 w;
+    w.x = vals[c8 * 8 + 0] | (static_cast<uint32_t>(vals[c8 * 8 + 1]) << 16);
+    w.y = vals[c8 * 8 + 2] | (static_cast<uint32_t>(vals[c8 * 8 + 3]) << 16);
+    w.z = vals[c8 * 8 + 4] | (static_cast<uint32_t>(vals[c8 * 8 + 5]) << 16);
+    w.w = vals[c8 * 8 + 6] | (static_cast<uint32_t>(vals[c8 * 8 + 7]) << 16);
+    *reinterpret_cast<uint4*>(tout + (c8 * 16 + (tid >> 3)) * 64 + (tid & 7) * 8) = w;
+  }
+}
+
+// ------------------------------------------------------------------ SIMT kernel
 template <typename T, int MP, ProjOut MODE>
 __global__ void __launch_bounds__(128) project_kernel(const ProjParams p) {
   extern __shared__ float psm[];
@@ -65,7 +133,8 @@ __global__ void __launch_bounds__(128) project_kernel(const ProjParams p) {
     const int l = i / MP, k = i % MP;
     Ps[i] = k < m ? to_f(P[l * m + k]) : 0.f;
   }
-  const T* x = static_cast<const T*>(which == 0 ? p.x[0] : p.x[1]) + static_cast<size_t>(bh) * p.N * d;
+  const T* x = static_cast<const T*>(which == 0 ? p.x[0] : p.x[1]) +
+               static_cast<size_t>(bh) * p.N * d;
   const int row0 = tile * kTileRows;
 
   float acc[MP];
@@ -89,68 +158,114 @@ __global__ void __launch_bounds__(128) project_kernel(const ProjParams p) {
     }
   }
 
-  const int row = row0 + tid;
   if constexpr (MODE == ProjOut::F32) {
+    const int row = row0 + tid;
     if (row < p.N) {
-      float* o = static_cast<float*>(which == 0 ? p.out[0] : p.out[1]) + (static_cast<size_t>(bh) * p.N + row) * m;
+      float* o = static_cast<float*>(which == 0 ? p.out[0] : p.out[1]) +
+                 (static_cast<size_t>(bh) * p.N + row) * m;
 #pragma unroll
       for (int k = 0; k < MP; ++k)
         if (k < m) o[k] = acc[k];
     }
   } else {
-    constexpr int KD = MODE == ProjOut::BF16X3 ? 3 * MP : MP;
-    uint16_t* tout = static_cast<uint16_t*>(which == 0 ? p.out[0] : p.out[1]) +
-                     (static_cast<size_t>(bh) * p.NT + tile) * (kTileRows * KD);
-    const float sc = which == 0 ? p.qscale : 1.f;
-#pragma unroll
-    for (int k = 0; k < MP; ++k) acc[k] *= sc;
-
-    uint16_t vals[KD];
-    if constexpr (MODE == ProjOut::F16X1) {
-      float amax = 0.f;
-#pragma unroll
-      for (int k = 0; k < MP; ++k) amax = fmaxf(amax, fabsf(acc[k]));
-      if (which == 1) {  // one exponent for the whole K tile
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if ((tid & 31) == 0) red[tid >> 5] = amax;
-        __syncthreads();
-        amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-      }
-      const int e = range_exponent(amax);
-      const float down = pow2i(-e);
-#pragma unroll
-      for (int k = 0; k < MP; ++k) vals[k] = f16_bits(acc[k] * down);
-      if (which == 0)
-        p.mul[0][static_cast<size_t>(bh) * p.NT * kTileRows + row] = pow2i(e);
-      else if (tid == 0)
-        p.mul[1][static_cast<size_t>(bh) * p.NT + tile] = pow2i(e);
-    } else {
-#pragma unroll
-      for (int k = 0; k < MP; ++k) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(acc[k]);
-        const uint16_t hib = __bfloat16_as_ushort(hi);
-        const uint16_t lob = bf16_bits(acc[k] - __bfloat162float(hi));
-        vals[k] = hib;                                   // segment 0: hi for both
-        vals[MP + k] = which == 0 ? hib : lob;           // Q: hi, K: lo
-        vals[2 * MP + k] = which == 0 ? lob : hib;       // Q: lo, K: hi
-      }
-      if (which == 0)
-        p.mul[0][static_cast<size_t>(bh) * p.NT * kTileRows + row] = 1.f;
-      else if (tid == 0)
-        p.mul[1][static_cast<size_t>(bh) * p.NT + tile] = 1.f;
-    }
-    // interleaved core-matrix layout: 8 columns (16 bytes) per store
-#pragma unroll
-    for (int c8 = 0; c8 < KD / 8; ++c8) {
-      uint4 w;
-      w.x = vals[c8 * 8 + 0] | (static_cast<uint32_t>(vals[c8 * 8 + 1]) << 16);
-      w.y = vals[c8 * 8 + 2] | (static_cast<uint32_t>(vals[c8 * 8 + 3]) << 16);
-      w.z = vals[c8 * 8 + 4] | (static_cast<uint32_t>(vals[c8 * 8 + 5]) << 16);
-      w.w = vals[c8 * 8 + 6] | (static_cast<uint32_t>(vals[c8 * 8 + 7]) << 16);
-      *reinterpret_cast<uint4*>(tout + (c8 * 16 + (tid >> 3)) * 64 + (tid & 7) * 8) = w;
-    }
+    store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red);
   }
+}
+
+// ------------------------------------------------------------------ tcgen05 kernel
+constexpr uint64_t kProjWaitNs = 2000000000ull;
+
+template <int MP>
+struct ProjTcPlan {
+  static constexpr int kCols = MP < 32 ? 32 : MP;   // TMEM columns (power of 2 >= 32)
+  static constexpr int kXBox = kTileRows * 64 * 2;  // one 64-column TMA box: 16 KB
+};
+
+// X tile (128 rows x d, bf16) by TMA into DCH boxes of [128][64] with 128-byte
+// swizzle; B = P_h^T (MP x 64*DCH) in the interleaved K-major layout.
+template <int MP, int DCH, ProjOut MODE>
+__global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
+                                                         const __grid_constant__ CUtensorMap xq,
+                                                         const __grid_constant__ CUtensorMap xk) {
+  using namespace ptx;
+  using Plan = ProjTcPlan<MP>;
+  constexpr int DP = DCH * 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sX = smem;  // DCH * 16 KB
+  uint16_t* sB = reinterpret_cast<uint16_t*>(smem + DCH * Plan::kXBox);  // MP * DP
+  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float red[4];
+  const int tile = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const CUtensorMap* xmap = which == 0 ? &xq : &xk;
+
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_sh, Plan::kCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar_load, DCH * Plan::kXBox);
+#pragma unroll
+    for (int c = 0; c < DCH; ++c)
+      tma_load_3d(sX + c * Plan::kXBox, xmap, c * 64, tile * kTileRows, bh, &bar_load);
+  }
+  // B operand: element (n, k) = P_h[k][n] at ((k/8)*(MP/8) + n/8)*64 + (n%8)*8 + k%8
+  const __nv_bfloat16* P =
+      static_cast<const __nv_bfloat16*>(p.P) + static_cast<size_t>(bh % p.H) * p.d * p.m;
+  for (int i = tid; i < MP * DP; i += 128) {
+    const int k = i / MP, n = i % MP;
+    const uint16_t v = k < p.d ? __bfloat16_as_ushort(P[k * p.m + n]) : uint16_t(0);
+    sB[((k >> 3) * (MP / 8) + (n >> 3)) * 64 + (n & 7) * 8 + (k & 7)] = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base_sh;
+
+  bool ok = __syncthreads_and(mbar_wait(&bar_load, 0, kProjWaitNs));
+  if (ok && tid == 0) {
+    constexpr uint32_t idesc = idesc_f16(128, MP, kFmtBF16, 0, 0);
+    tc_fence_after();
+#pragma unroll
+    for (int s = 0; s < DP / 16; ++s) {
+      const uint64_t ad = smem_desc(smem_u32(sX) + (s >> 2) * Plan::kXBox + (s & 3) * 32, 16,
+                                    1024, kLayoutSwizzle128);
+      const uint64_t bd = smem_desc(smem_u32(sB) + s * 2 * (MP / 8) * 128, (MP / 8) * 128, 128,
+                                    kLayoutInterleave);
+      mma_ss(tb, ad, bd, idesc, s > 0);
+    }
+    mma_commit(&bar_mma);
+  }
+  if (ok) ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kProjWaitNs));
+  if (ok) {
+    tc_fence_after();
+    float acc[MP];
+#pragma unroll
+    for (int c = 0; c < MP; c += 16) {
+      uint32_t r[16];
+      tmem_ld16(tb + (static_cast<uint32_t>(warp * 32) << 16) + c, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(r[i]);
+    }
+    store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red);
+  } else {
+    if (tid == 0) atomicExch(p.err, 1);
+    // the TMA copy or the MMA may still be in flight: let it finish before exit
+    mbar_wait(&bar_load, 0, kProjWaitNs);
+    if (tid == 0) mma_commit(&bar_mma);
+    mbar_wait(&bar_mma, 0, kProjWaitNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, Plan::kCols);
 }
 
 template <typename T, int MP, ProjOut MODE>
@@ -167,6 +282,33 @@ cudaError_t launch_one(const ProjParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int MP, int DCH, ProjOut MODE>
+cudaError_t launch_tc_one(const ProjParams& p, cudaStream_t stream) {
+  using Plan = ProjTcPlan<MP>;
+  auto kern = project_tc_kernel<MP, DCH, MODE>;
+  int smem = DCH * Plan::kXBox + MP * DCH * 64 * 2 + 1024;
+  // never more CTAs per SM than their TMEM allocations fit in 512 columns
+  const int max_ctas = 512 / Plan::kCols;
+  const int min_smem = 233472 / (max_ctas + 1) + 1;  // 228 KB of shared memory per SM
+  if (smem < min_smem) smem = min_smem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.NT, p.BH, p.nx);
+  kern<<<grid, 128, smem, stream>>>(p, p.xmap[0], p.xmap[1]);
+  return cudaGetLastError();
+}
+
+template <int MP, ProjOut MODE>
+cudaError_t launch_tc_mp(const ProjParams& p, cudaStream_t stream) {
+  switch ((p.d + 63) / 64) {
+    case 1: return launch_tc_one<MP, 1, MODE>(p, stream);
+    case 2: return launch_tc_one<MP, 2, MODE>(p, stream);
+    case 3: return launch_tc_one<MP, 3, MODE>(p, stream);
+    case 4: return launch_tc_one<MP, 4, MODE>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <typename T>
 cudaError_t launch_f32_out(const ProjParams& p, cudaStream_t stream) {
   if (p.m <= 16) return launch_one<T, 16, ProjOut::F32>(p, stream);
@@ -177,18 +319,30 @@ cudaError_t launch_f32_out(const ProjParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+bool project_tc_eligible(const ProjParams& p) {
+  return p.bf16_in && p.mode != ProjOut::F32 && p.d % 8 == 0 && p.d <= 256;
+}
+
 cudaError_t launch_project(const ProjParams& p, cudaStream_t stream) {
   if (p.mode == ProjOut::F32)
     return p.bf16_in ? launch_f32_out<__nv_bfloat16>(p, stream) : launch_f32_out<float>(p, stream);
   if (!p.bf16_in) return cudaErrorInvalidValue;
+  const bool tc = p.use_tc && project_tc_eligible(p);
   if (p.mode == ProjOut::BF16X3) {
-    if (p.m == 16) return launch_one<__nv_bfloat16, 16, ProjOut::BF16X3>(p, stream);
-    return cudaErrorInvalidValue;
+    if (p.m != 16) return cudaErrorInvalidValue;
+    return tc ? launch_tc_mp<16, ProjOut::BF16X3>(p, stream)
+              : launch_one<__nv_bfloat16, 16, ProjOut::BF16X3>(p, stream);
   }
   switch (p.m) {
-    case 32: return launch_one<__nv_bfloat16, 32, ProjOut::F16X1>(p, stream);
-    case 64: return launch_one<__nv_bfloat16, 64, ProjOut::F16X1>(p, stream);
-    case 128: return launch_one<__nv_bfloat16, 128, ProjOut::F16X1>(p, stream);
+    case 32:
+      return tc ? launch_tc_mp<32, ProjOut::F16X1>(p, stream)
+                : launch_one<__nv_bfloat16, 32, ProjOut::F16X1>(p, stream);
+    case 64:
+      return tc ? launch_tc_mp<64, ProjOut::F16X1>(p, stream)
+                : launch_one<__nv_bfloat16, 64, ProjOut::F16X1>(p, stream);
+    case 128:
+      return tc ? launch_tc_mp<128, ProjOut::F16X1>(p, stream)
+                : launch_one<__nv_bfloat16, 128, ProjOut::F16X1>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -135,11 +135,36 @@ spa::ProjParams proj_params(const void* q, const void* k, const void* P, int B, 
   return pp;
 }
 
+// 3-D (inner, N, BH) bf16 tensor map with 128-byte swizzle and a 64 x 128 box.
+int encode_rows_map(CUtensorMap* map, const void* base, int inner, int N, int BH) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  int st = get_encode(&encode);
+  if (st) return st;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
+                           static_cast<cuuint64_t>(N) * inner * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(spa::kTileRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SPA_ERR_CUDA;
+  return SPA_OK;
+}
+
 // Stage 1: projection of q and k into the workspace.
 int run_prepare(const void* q, const void* k, const void* P, int B, int H, int N, int d, int m,
                 int dtype, void* ws, cudaStream_t stream) {
   const Layout L = make_layout(B, H, N, m, dtype);
-  const spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, dtype, L, static_cast<char*>(ws));
+  spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, dtype, L, static_cast<char*>(ws));
+  pp.use_tc = 1;
+  if (spa::project_tc_eligible(pp)) {
+    int st;
+    if ((st = encode_rows_map(&pp.xmap[0], q, d, N, B * H))) return st;
+    if ((st = encode_rows_map(&pp.xmap[1], k, d, N, B * H))) return st;
+    if ((st = device_error_ptr(&pp.err))) return st;
+  }
   return cuda_status(spa::launch_project(pp, stream));
 }
 
@@ -164,19 +189,8 @@ int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int
     return cuda_status(spa::launch_attn_f32(ap, stream));
   }
   int st;
-  PFN_cuTensorMapEncodeTiled_v12000 encode;
-  if ((st = get_encode(&encode))) return st;
   spa::AttnTcParams ap{};
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(N),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dv) * 2,
-                           static_cast<cuuint64_t>(N) * dv * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(spa::kTileRows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  if (encode(&ap.vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return SPA_ERR_CUDA;
+  if ((st = encode_rows_map(&ap.vmap, v, dv, N, BH))) return st;
   int* err = nullptr;
   if ((st = device_error_ptr(&err))) return st;
   ap.Qs = reinterpret_cast<const uint16_t*>(w + L.qs);

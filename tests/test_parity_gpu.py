@@ -86,6 +86,8 @@ SMALL = [
     (2, 2, 384, 64, 16, 128, False),
     (1, 1, 777, 128, 128, 128, True),
     (1, 1, 300, 256, 32, 64, False),
+    (1, 2, 200, 60, 32, 64, True),     # d not a multiple of 8: SIMT projection
+    (1, 1, 333, 72, 16, 128, False),   # ragged 64-column box in the TMA projection
 ]
 
 
