@@ -5,8 +5,9 @@
 // streams the key/value tiles of that head once for both.  Ten warps:
 //   warps 0-3  softmax for query tile 0   (TMEM lanes 0-127 of S0 / O0)
 //   warps 4-7  softmax for query tile 1   (TMEM lanes 0-127 of S1 / O1)
-//   warp  8    loads: the two Qp tiles once, then a ring of STAGES Kp tiles
-//              (one bulk copy each) and V tiles (TMA, 128-byte swizzle)
+//   warp  8    loads: the two Qp tiles once, then a ring of STAGES slots, each
+//              a Kp tile (one bulk copy) and a V tile (TMA, 128-byte swizzle)
+//              completing on one barrier
 //   warp  9    tensor-memory allocation and tcgen05.mma issue
 // Tensor memory (512 columns):  S0 | S1 | O0 | O1, with the bf16 probabilities
 // P_t written over the first 64 columns of S_t and read from there by the PV
@@ -17,6 +18,11 @@
 // order, so S_t(j+1) never overwrites P_t(j) before PV_t(j) has read it, and
 // the commit that signals "S_t(j+1) ready" also covers PV_t(j), which lets the
 // softmax rescale O_t right after it without another wait.
+// Issuing one tcgen05.mma costs the issuing thread about as long as a
+// 128x128x16 MMA takes to execute, so the issuer does as little else as
+// possible: one ring barrier per slot (not separate K and V barriers), three
+// commits per key tile, and a key loop unrolled by the ring depth so every
+// shared-memory descriptor offset is a compile-time constant.
 //
 // Online softmax (base 2, log2(e)/sqrt(m) already folded into Qp): the
 // running max only moves when a tile's max exceeds it by more than 8; in
@@ -65,7 +71,7 @@ struct WsPlan {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+  uint64_t kv_full[3], kv_empty[3];
   uint64_t s_full[2], p_full[2];
   uint64_t o_final;
   uint64_t drain;
@@ -108,10 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars.q_full, 1);
     for (int s = 0; s < S; ++s) {
-      mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
-      mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.v_empty[s], 1);
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
@@ -138,30 +142,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_g2s(smem + Plan::kQ, Qs, Plan::kQBytes, &bars.q_full);
       if (nkv1 > 0) bulk_g2s(smem + Plan::kQ + Plan::kQBytes, Qs + kTileElems, Plan::kQBytes,
                              &bars.q_full);
-      int armed_k = 0, armed_v = 0;  // steps whose K / V copies were started
+      int armed = 0;  // key tiles whose copies were started
       for (int j = 0; j < nkv; ++j) {
         const int slot = j % S;
         const uint32_t ph = (j / S) & 1;
-        if (j >= S && !wait_or_abort(&bars.k_empty[slot], ph ^ 1, &abort_sh, p.err)) break;
-        mbar_arrive_expect_tx(&bars.k_full[slot], Plan::kKBytes);
+        if (j >= S && !wait_or_abort(&bars.kv_empty[slot], ph ^ 1, &abort_sh, p.err)) break;
+        mbar_arrive_expect_tx(&bars.kv_full[slot], Plan::kKBytes + Plan::kVBytes);
         bulk_g2s(smem + Plan::kK + slot * Plan::kKBytes, Ks + static_cast<size_t>(j) * kTileElems,
-                 Plan::kKBytes, &bars.k_full[slot]);
-        armed_k = j + 1;
-        if (j >= S && !wait_or_abort(&bars.v_empty[slot], ph ^ 1, &abort_sh, p.err)) break;
-        mbar_arrive_expect_tx(&bars.v_full[slot], Plan::kVBytes);
+                 Plan::kKBytes, &bars.kv_full[slot]);
         uint8_t* vdst = smem + Plan::kV + slot * Plan::kVBytes;
 #pragma unroll
         for (int h = 0; h < DV / 64; ++h)
-          tma_load_3d(vdst + h * 16384, &vmap, h * 64, j * kTileRows, bh, &bars.v_full[slot]);
-        armed_v = j + 1;
+          tma_load_3d(vdst + h * 16384, &vmap, h * 64, j * kTileRows, bh, &bars.kv_full[slot]);
+        armed = j + 1;
       }
       if (abort_sh) {
         // let every copy this thread started land before the CTA's memory is reused
         mbar_wait(&bars.q_full, 0, kLimitNs);
-        for (int j = max(0, armed_k - S); j < armed_k; ++j)
-          mbar_wait(&bars.k_full[j % S], (j / S) & 1, kLimitNs);
-        for (int j = max(0, armed_v - S); j < armed_v; ++j)
-          mbar_wait(&bars.v_full[j % S], (j / S) & 1, kLimitNs);
+        for (int j = max(0, armed - S); j < armed; ++j)
+          mbar_wait(&bars.kv_full[j % S], (j / S) & 1, kLimitNs);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -169,60 +168,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16(128, 128, F16OPS ? kFmtF16 : kFmtBF16, 0, 0);
       constexpr uint32_t kIdescPV = idesc_f16(128, DV, kFmtBF16, 0, 1);
-      const uint32_t sQ0 = smem_u32(smem + Plan::kQ), sQ1 = sQ0 + Plan::kQBytes;
-      const uint32_t sK = smem_u32(smem + Plan::kK), sV = smem_u32(smem + Plan::kV);
-      auto issue_s = [&](int t, int slot) {
-        const uint32_t a = t == 0 ? sQ0 : sQ1;
-        const uint32_t b = sK + slot * Plan::kKBytes;
+      // descriptor bases; per-slot and per-k-step offsets below are constants
+      const uint64_t dQ0 = smem_desc(smem_u32(smem + Plan::kQ), 2048, 128, kLayoutInterleave);
+      const uint64_t dK = smem_desc(smem_u32(smem + Plan::kK), 2048, 128, kLayoutInterleave);
+      const uint64_t dV = smem_desc(smem_u32(smem + Plan::kV), 16384, 1024, kLayoutSwizzle128);
+      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K_slot^T, then signal the softmax
+        const uint64_t a = dQ0 + static_cast<uint64_t>((t * Plan::kQBytes) >> 4);
+        const uint64_t b = dK + static_cast<uint64_t>((slot * Plan::kKBytes) >> 4);
         const uint32_t d = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
 #pragma unroll
-        for (int s = 0; s < KD / 16; ++s)
-          mma_ss(d, smem_desc(a + s * 4096, 2048, 128, kLayoutInterleave),
-                 smem_desc(b + s * 4096, 2048, 128, kLayoutInterleave), kIdescS, s > 0);
+        for (int k = 0; k < KD / 16; ++k)
+          mma_ss(d, a + (k * 4096 >> 4), b + (k * 4096 >> 4), kIdescS, k > 0);
         mma_commit(&bars.s_full[t]);
       };
-      auto issue_pv = [&](int t, int slot, bool acc) {
+      auto issue_pv = [&](int t, int slot, uint32_t acc) {  // O_t += P_t V_slot
         const uint32_t a = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
         const uint32_t d = tb + (t == 0 ? Plan::kColsO0 : Plan::kColsO1);
-        const uint32_t b = sV + slot * Plan::kVBytes;
+        const uint64_t b = dV + static_cast<uint64_t>((slot * Plan::kVBytes) >> 4);
+        mma_ts(d, a, b, kIdescPV, acc);
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_ts(d, a + s * 8, smem_desc(b + s * 2048, 16384, 1024, kLayoutSwizzle128), kIdescPV,
-                 (acc || s > 0) ? 1u : 0u);
+        for (int k = 1; k < 8; ++k) mma_ts(d, a + k * 8, b + (k * 2048 >> 4), kIdescPV, 1u);
       };
       bool ok = wait_or_abort(&bars.q_full, 0, &abort_sh, p.err) &&
-                wait_or_abort(&bars.k_full[0], 0, &abort_sh, p.err);
+                wait_or_abort(&bars.kv_full[0], 0, &abort_sh, p.err);
       if (ok) {
         tc_fence_after();
-        if (nkv0 > 0) issue_s(0, 0);
+        issue_s(0, 0);
         if (nkv1 > 0) issue_s(1, 0);
-        mma_commit(&bars.k_empty[0]);
       }
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int slot = j % S;
-        const uint32_t ph = (j / S) & 1;
-        if (!(ok = wait_or_abort(&bars.v_full[slot], ph, &abort_sh, p.err))) break;
-        if (j < nkv0) {
-          if (!(ok = wait_or_abort(&bars.p_full[0], j & 1, &abort_sh, p.err))) break;
-          tc_fence_after();
-          issue_pv(0, slot, j > 0);
-        }
-        const int jn = j + 1;
-        const int slotn = jn % S;
-        if (jn < nkv) {
-          if (!(ok = wait_or_abort(&bars.k_full[slotn], (jn / S) & 1, &abort_sh, p.err))) break;
-          tc_fence_after();
-          if (jn < nkv0) issue_s(0, slotn);
-        }
-        if (j < nkv1) {
-          if (!(ok = wait_or_abort(&bars.p_full[1], j & 1, &abort_sh, p.err))) break;
-          tc_fence_after();
-          issue_pv(1, slot, j > 0);
-        }
-        mma_commit(&bars.v_empty[slot]);
-        if (jn < nkv) {
-          if (jn < nkv1) issue_s(1, slotn);
-          mma_commit(&bars.k_empty[slotn]);
+      // key tiles in groups of S so that slot = u is a compile-time constant
+      for (int j0 = 0; ok && j0 < nkv; j0 += S) {
+#pragma unroll
+        for (int u = 0; u < S; ++u) {
+          const int j = j0 + u;
+          if (!ok || j >= nkv) break;
+          const int un = (u + 1) % S;                               // slot of key tile j+1
+          const uint32_t phn = ((j0 / S) + (u + 1 == S ? 1 : 0)) & 1;  // its ring phase
+          const bool next = j + 1 < nkv;
+          if (j < nkv0) {
+            if (!(ok = wait_or_abort(&bars.p_full[0], j & 1, &abort_sh, p.err))) break;
+            tc_fence_after();
+            issue_pv(0, u, j > 0 ? 1u : 0u);
+          }
+          if (next) {
+            if (!(ok = wait_or_abort(&bars.kv_full[un], phn, &abort_sh, p.err))) break;
+            tc_fence_after();
+            if (j + 1 < nkv0) issue_s(0, un);
+          }
+          if (j < nkv1) {
+            if (!(ok = wait_or_abort(&bars.p_full[1], j & 1, &abort_sh, p.err))) break;
+            tc_fence_after();
+            issue_pv(1, u, j > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars.kv_empty[u]);  // both tiles are done with K(j) and V(j)
+          if (next && j + 1 < nkv1) issue_s(1, un);
         }
       }
       mma_commit(ok ? &bars.o_final : &bars.drain);

@@ -88,6 +88,11 @@ SMALL = [
     (1, 1, 300, 256, 32, 64, False),
     (1, 2, 200, 60, 32, 64, True),     # d not a multiple of 8: SIMT projection
     (1, 1, 333, 72, 16, 128, False),   # ragged 64-column box in the TMA projection
+    # an odd number of 128-row tiles leaves the last CTA with one query tile,
+    # with two- (m=128) and three-stage (m<128) key/value rings
+    (2, 2, 777, 64, 128, 64, False),
+    (1, 1, 1281, 128, 32, 128, False),
+    (1, 2, 1281, 128, 64, 128, True),
 ]
 
 
