@@ -199,29 +199,35 @@ def physical_device(local_rank: int) -> str:
 
 # ------------------------------------------------------------------ oracle (CPU)
 def oracle_sample(w, q, k, v, P, target_s: float):
-    """Time the fp64 oracle on head 0 of the workload, with as many query rows as
-    fit in about target_s seconds.  Returns (flops, seconds, rows, threads)."""
+    """Time the fp64 oracle on a bounded sample of the workload: query rows of
+    head 0 (evenly spaced) and, when every row of one head fits in the time,
+    whole heads.  Returns (flops, seconds, description, threads)."""
     import numpy as np
 
     import oracle
-    q0, k0, v0 = (t[:1, :1].contiguous() for t in (q, k, v))
-    P0 = P[:1].contiguous()
 
-    def run(rows):
+    def run(heads, rows):
         idx = np.linspace(0, w.N - 1, rows).round().astype(np.int64)
-        t = time.perf_counter()
-        oracle.attention(q0, k0, v0, P0, causal=w.causal, rows=idx)
-        dt = time.perf_counter() - t
-        keys = (idx + 1).sum() if w.causal else rows * w.N
-        fl = 2.0 * w.N * w.d * w.m + 2.0 * rows * w.d * w.m + 2.0 * float(keys) * (w.m + w.dv)
+        qs, ks, vs = (t[:1, :heads].contiguous() for t in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.attention(qs, ks, vs, P[:heads].contiguous(), causal=w.causal, rows=idx)
+        dt = time.perf_counter() - t0
+        keys = float((idx + 1).sum()) if w.causal else float(rows) * w.N
+        fl = heads * (2.0 * w.N * w.d * w.m + 2.0 * rows * w.d * w.m + 2.0 * keys * (w.m + w.dv))
         return fl, dt
 
-    _, t1 = run(1)
-    _, t64 = run(64)
+    _, t1 = run(1, 1)
+    _, t64 = run(1, 64)
     per_row = max((t64 - t1) / 63.0, 1e-6)
     rows = int(max(1, min(w.N, (target_s - t1) / per_row)))
-    fl, dt = run(rows)
-    return fl, dt, rows, oracle.num_threads()
+    heads = 1
+    if rows == w.N:
+        per_head = t1 + w.N * per_row
+        heads = int(max(1, min(w.H, target_s / per_head)))
+    fl, dt = run(heads, rows)
+    desc = (f"{heads} of {w.H} heads, {rows} of {w.N} query rows each (evenly spaced), full key "
+            f"range, projection of all keys of those heads; {dt:.1f} s")
+    return fl, dt, desc, oracle.num_threads()
 
 
 # ------------------------------------------------------------------ arms
@@ -252,24 +258,16 @@ def run_reference(args, rank, world):
     q, k, v = si.make_qkv(w)
     P = si.make_P(w)
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    import numpy as np
-
-    import oracle
-    q0, k0, v0 = (t[:1, :1].contiguous() for t in (q, k, v))
-    P0 = P[:1].contiguous()
-    # size one step: rows of head 0 that take about per_step seconds
-    fl_cal, t_cal, rows, threads = oracle_sample(w, q, k, v, P, per_step)
-    idx = np.linspace(0, w.N - 1, rows).round().astype(np.int64)
-    fl_step = 2.0 * w.N * w.d * w.m + 2.0 * rows * w.d * w.m + 2.0 * rows * w.N * (w.m + w.dv)
+    # each step is one bounded sample of about per_step seconds
     for _ in range(args.warmup):
-        oracle.attention(q0, k0, v0, P0, causal=w.causal, rows=idx)
-    t = time.perf_counter()
+        oracle_sample(w, q, k, v, P, per_step)
+    fl_tot = dt = 0.0
     for _ in range(args.steps):
-        oracle.attention(q0, k0, v0, P0, causal=w.causal, rows=idx)
-    dt = time.perf_counter() - t
-    value = fl_step * args.steps / dt / 1e12
-    sample = (f"head 0 of {w.H}, {rows} of {w.N} query rows (evenly spaced) per step, "
-              f"full key range; projection of all {w.N} keys of the head included")
+        fl, t1, sample, threads = oracle_sample(w, q, k, v, P, per_step)
+        fl_tot += fl
+        dt += t1
+    value = fl_tot / dt / 1e12
+    sample = "per step: " + sample
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
@@ -376,10 +374,9 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        fl, dt, rows, threads = oracle_sample(w, q_h, k_h, v_h, P_h, args.cpu_seconds)
+        fl, dt, desc, threads = oracle_sample(w, q_h, k_h, v_h, P_h, args.cpu_seconds)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"head 0 of {w.H}, {rows} of {w.N} query rows (evenly spaced), full "
-                         f"key range, projection of all keys of the head; {dt:.1f} s"}
+               "sample": desc}
 
     if rank == 0:
         peak, peak_sus, peak_src = load_peaks()
