@@ -9,6 +9,7 @@
 //              a Kp tile (one bulk copy) and a V tile (TMA, 128-byte swizzle)
 //              completing on one barrier
 //   warp  9    tensor-memory allocation and tcgen05.mma issue
+//   warps 10-11 idle (they complete the control warpgroup for the register split)
 // Tensor memory (512 columns):  S0 | S1 | O0 | O1, with the bf16 probabilities
 // P_t written over the first 64 columns of S_t and read from there by the PV
 // product.  The MMA issue order per key tile j is
@@ -44,7 +45,13 @@ namespace {
 using namespace ptx;
 
 constexpr uint64_t kLimitNs = 2000000000ull;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // three warpgroups
+// Register split.  The block is launched with 384 x 168 registers; the control
+// warpgroup (warps 8-11) gives up most of its share and each softmax
+// warpgroup takes 184: 128 * (184 + 184 + 128) = 63488 <= 64512.  Each
+// warpgroup executes its setmaxnreg once, at the top of its branch.
+constexpr uint32_t kRegsSoftmax = 184;
+constexpr uint32_t kRegsControl = 128;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
@@ -131,8 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tb = tmem_base_sh;
   constexpr int kTileElems = kTileRows * KD;
-
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   setmaxnreg_dec<kRegsControl>();  // the whole control warpgroup
+   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
       prefetch_tmap(&vmap);
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&bars.kv_full[j % S], (j / S) & 1, kLimitNs);
       }
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16(128, 128, F16OPS ? kFmtF16 : kFmtBF16, 0, 0);
@@ -227,8 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(ok ? &bars.o_final : &bars.drain);
       if (!ok) mbar_wait(&bars.drain, 0, kLimitNs);  // own MMAs in flight
     }
+   }  // warps 10-11: no role
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    setmaxnreg_inc<kRegsSoftmax>();  // the whole softmax warpgroup
     const int t = warp >> 2;  // query tile of this warpgroup
     const int r = tid & 127;  // row within the tile == TMEM lane
     const int nkv_t = t == 0 ? nkv0 : nkv1;
@@ -268,33 +278,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = c < kvalid ? x[c] : -INFINITY;
       }
-      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+      // row max: eight independent chains of three-input maxima
+      float mx[8];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
-        mx2 = fmaxf(mx2, x[c + 2]);
-        mx3 = fmaxf(mx3, x[c + 3]);
+      for (int i = 0; i < 8; ++i) {
+        float mi = max3(x[16 * i], x[16 * i + 1], x[16 * i + 2]);
+#pragma unroll
+        for (int k = 3; k < 15; k += 2) mi = max3(mi, x[16 * i + k], x[16 * i + k + 1]);
+        mx[i] = fmaxf(mi, x[16 * i + 15]);
       }
+      const float rmax = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
+                              fmaxf(mx[6], mx[7]));
       const float mult = qm * km;  // > 0: range exponents times log2(e)/sqrt(m)
-      const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mult;
+      const float tmax = rmax * mult;
       const bool grow = tmax > m_run + kRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
         alpha = ex2(m_run - tmax);  // 0 on the first tile
         m_run = tmax;
       }
-      const float neg_m = -m_run;
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      // p = 2^(s * mult - m): scale and shift two at a time, exp2 on the MUFU,
+      // row sum in packed pairs, bf16x2 straight into the S columns of TMEM
+      const uint64_t mult2 = pack_f32x2(mult, mult);
+      const uint64_t negm2 = pack_f32x2(-m_run, -m_run);
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = h * 32 + 2 * i;
-          const float e0 = ex2(fmaf(x[c], mult, neg_m));
-          const float e1 = ex2(fmaf(x[c + 1], mult, neg_m));
-          if (i & 1) { s2 += e0; s3 += e1; } else { s0 += e0; s1 += e1; }
+          float y0, y1;
+          unpack_f32x2(fma_f32x2(pack_f32x2(x[c], x[c + 1]), mult2, negm2), y0, y1);
+          const float e0 = ex2(y0), e1 = ex2(y1);
+          sum2[i & 3] = add_f32x2(sum2[i & 3], pack_f32x2(e0, e1));
           pk[i] = pack_bf16x2(e0, e1);
         }
         tmem_st16(tS + h * 16, pk);
@@ -312,7 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(tO + c0, v);
         }
       }
-      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+      float lsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a, b;
+        unpack_f32x2(sum2[i], a, b);
+        lsum += a + b;
+      }
+      l_run = l_run * alpha + lsum;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars.p_full[t]);
