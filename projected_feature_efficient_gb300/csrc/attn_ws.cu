@@ -26,9 +26,10 @@
 // shared-memory descriptor offset is a compile-time constant.
 //
 // Online softmax (base 2, log2(e)/sqrt(m) already folded into Qp): the
-// running max only moves when a tile's max exceeds it by more than 8; in
-// between, probabilities up to 2^8 are accumulated, which leaves the final
-// O / l unchanged up to rounding and skips most rescales of O.
+// running max only moves when a tile's max exceeds it by more than 20; in
+// between, probabilities up to 2^20 are accumulated (finite in bf16 and fp32,
+// same relative precision), which leaves the final O / l unchanged up to
+// rounding and skips almost every rescale of O.
 //
 // Every wait is bounded (2 s).  A role that gives up sets the CTA abort flag
 // and the device error word; every role leaves its loop, the MMA issuer and
@@ -54,7 +55,7 @@ constexpr uint32_t kRegsSoftmax = 184;
 constexpr uint32_t kRegsControl = 128;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr float kRescaleThreshold = 20.f;  // log2 units: p <= 2^20 between rescales
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
@@ -84,8 +85,11 @@ struct Bars {
   uint64_t drain;
 };
 
+// Bounded wait that also gives up once another role of the CTA has aborted.
+// The common case (phase already complete) costs one try_wait.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
                                               int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (*abort) return false;
   if (mbar_wait(bar, parity, kLimitNs)) return true;
   *abort = 1;
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.p_full[t], 4);  // one arrival per softmax warp
     }
     mbar_init(&bars.o_final, 1);
     mbar_init(&bars.drain, 1);
@@ -320,13 +324,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S(j) commit) and PV(j) waits for p_full below.
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tO + c0, v);
+        for (int c0 = 0; c0 < DV; c0 += 64) {  // 64 columns per round trip
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tO + c0, v0);
+          tmem_ld32(tO + c0 + 32, v1);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st16(tO + c0, v);
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = __float_as_uint(__uint_as_float(v0[i]) * alpha);
+            v1[i] = __float_as_uint(__uint_as_float(v1[i]) * alpha);
+          }
+          tmem_st32(tO + c0, v0);
+          tmem_st32(tO + c0 + 32, v1);
         }
       }
       float lsum = 0.f;
@@ -339,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * alpha + lsum;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars.p_full[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[t]);
     }
     // epilogue: O / l -> out (fp32)
     if (ok && nkv_t > 0) {
