@@ -111,8 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NT = p.NT;
   const int NP = (NT + 1) >> 1;
-  const int bh = blockIdx.x / NP;
-  const int pair = NP - 1 - static_cast<int>(blockIdx.x % NP);  // longest causal work first
+  // Causal work grows with the pair index, so blocks go out longest first
+  // across all heads (pair-major); without a mask every block has the same
+  // work and head-major order keeps the blocks that share a head's K/V together.
+  const int bh = p.causal ? static_cast<int>(blockIdx.x % p.BH) : static_cast<int>(blockIdx.x / NP);
+  const int pair = NP - 1 - static_cast<int>(p.causal ? blockIdx.x / p.BH : blockIdx.x % NP);
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const int nkv0 = p.causal ? qt0 + 1 : NT;
   const int nkv1 = qt1 < NT ? (p.causal ? qt1 + 1 : NT) : 0;
