@@ -2,7 +2,8 @@
 // (bf16 inputs, fp16 or split-bf16 score operands, fp32 accumulation).
 //
 // One CTA owns two 128-row query tiles (t = 0, 1) of one (batch, head) and
-// streams the key/value tiles of that head once for both.  Ten warps:
+// streams the key/value tiles of that head once for both.  Twelve warps in
+// three warpgroups (setmaxnreg moves registers from the third to the first two):
 //   warps 0-3  softmax for query tile 0   (TMEM lanes 0-127 of S0 / O0)
 //   warps 4-7  softmax for query tile 1   (TMEM lanes 0-127 of S1 / O1)
 //   warp  8    loads: the two Qp tiles once, then a ring of STAGES slots, each
