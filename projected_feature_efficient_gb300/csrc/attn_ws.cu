@@ -75,6 +75,9 @@ struct WsPlan {
   static constexpr int kBytes = kV + kStages * kVBytes;
   // one CTA per SM: a second one would wait in tcgen05.alloc for the 512 columns
   static constexpr int kLaunch = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
+  // epilogue staging of one query tile's fp32 output, reusing the Q/K/V area
+  static constexpr int kStageBytes = kTileRows * DV * 4;
+  static_assert(2 * kStageBytes <= kBytes, "output staging must fit in the operand area");
   static constexpr uint32_t kColsS0 = 0, kColsS1 = 128, kColsO0 = 256, kColsO1 = 256 + DV;
 };
 
@@ -100,7 +103,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 template <int KD, int DV, bool F16OPS>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_ws_kernel(const AttnTcParams p, const __grid_constant__ CUtensorMap vmap) {
+    attn_ws_kernel(const AttnTcParams p, const __grid_constant__ CUtensorMap vmap,
+                   const __grid_constant__ CUtensorMap omap) {
   using Plan = WsPlan<KD, DV>;
   constexpr int S = Plan::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -152,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ loader
     if (lane == 0) {
       prefetch_tmap(&vmap);
+      prefetch_tmap(&omap);
       const uint16_t* Qs = p.Qs + (static_cast<size_t>(bh) * NT + qt0) * kTileElems;
       const uint16_t* Ks = p.Ks + static_cast<size_t>(bh) * NT * kTileElems;
       mbar_arrive_expect_tx(&bars.q_full, (nkv1 > 0 ? 2 : 1) * Plan::kQBytes);
@@ -355,27 +360,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full[t]);
     }
-    // epilogue: O / l -> out (fp32)
-    if (ok && nkv_t > 0) {
-      if (wait_or_abort(&bars.o_final, 0, &abort_sh, p.err)) {
+    // epilogue: O / l -> out (fp32), staged in shared memory and written by
+    // TMA stores.  Once o_final has fired every MMA is complete and every load
+    // consumed, so tile t stages its 128 x DV block over the operand area at
+    // t * kStageBytes, as DV/32 boxes of 128 rows x 128 B in the 128-byte
+    // swizzle of the output tensor map (16-byte chunk q of row r sits at chunk
+    // q ^ (r % 8)), which also spreads a warp's stores over all banks.  The
+    // store clips rows past N.  All 128 threads of the warpgroup reach the
+    // named barrier; a thread that gave up has set abort_sh before it.
+    if (nkv_t > 0) {
+      const uint32_t stage_base = ((smem_u32(smem_raw) + 1023u) & ~1023u) + t * Plan::kStageBytes;
+      if (ok && wait_or_abort(&bars.o_final, 0, &abort_sh, p.err)) {
         tc_fence_after();
         const float inv = 1.f / l_run;
-        float* dst = p.out + (static_cast<size_t>(bh) * p.N + row) * DV;
+        const uint32_t row_base = stage_base + r * 128;
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
 #pragma unroll
         for (int c0 = 0; c0 < DV; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tO + c0, v);
           tmem_wait_ld();
-          if (row < p.N) {
+          const uint32_t rb = row_base + (c0 / 32) * (kTileRows * 128);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              float4 o4 = make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                                      __uint_as_float(v[i + 2]) * inv,
-                                      __uint_as_float(v[i + 3]) * inv);
-              *reinterpret_cast<float4*>(dst + c0 + i) = o4;
-            }
-          }
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(rb + ((q ^ sw) << 4),
+                         __float_as_uint(__uint_as_float(v[4 * q]) * inv),
+                         __float_as_uint(__uint_as_float(v[4 * q + 1]) * inv),
+                         __float_as_uint(__uint_as_float(v[4 * q + 2]) * inv),
+                         __float_as_uint(__uint_as_float(v[4 * q + 3]) * inv));
         }
+        fence_proxy_async_smem();
+      }
+      if (t == 0) named_bar_sync(1, 128); else named_bar_sync(2, 128);
+      if (r == 0 && !abort_sh) {
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32)
+          tma_store_3d(&omap, stage_base + (c0 / 32) * (kTileRows * 128), c0, qt * kTileRows, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -393,7 +415,7 @@ cudaError_t launch_ws(const AttnTcParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long blocks = static_cast<long long>((p.NT + 1) / 2) * p.BH;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kThreads, Plan::kLaunch, stream>>>(p, p.vmap);
+  kern<<<static_cast<unsigned>(blocks), kThreads, Plan::kLaunch, stream>>>(p, p.vmap, p.omap);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,7 @@ struct AttnTcParams {
   const float* qmul;     // [BH][NT*128]
   const float* kmul;     // [BH][NT]
   CUtensorMap vmap;      // V as 3-D (d_v, N, BH), bf16, 128-byte swizzle, box (64,128,1)
+  CUtensorMap omap;      // out as 3-D (d_v, N, BH), fp32, 128-byte swizzle, box (32,128,1)
   float* out;            // [BH][N][d_v]
   int* err;              // device error word
   int BH, N, NT, KD, dv, causal;

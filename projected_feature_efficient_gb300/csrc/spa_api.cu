@@ -135,22 +135,28 @@ spa::ProjParams proj_params(const void* q, const void* k, const void* P, int B, 
   return pp;
 }
 
-// 3-D (inner, N, BH) bf16 tensor map with 128-byte swizzle and a 64 x 128 box.
-int encode_rows_map(CUtensorMap* map, const void* base, int inner, int N, int BH) {
+// Row-major [BH][N][inner] tensor as a 3-D tensor map with 128-byte swizzle and
+// 128-row boxes whose inner extent is 128 bytes (64 bf16 or 32 fp32 values).
+int encode_rows_map(CUtensorMap* map, const void* base, int inner, int N, int BH,
+                    CUtensorMapDataType type, int elem_bytes) {
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   int st = get_encode(&encode);
   if (st) return st;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
-                           static_cast<cuuint64_t>(N) * inner * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(spa::kTileRows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * elem_bytes,
+                           static_cast<cuuint64_t>(N) * inner * elem_bytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes),
+                       static_cast<cuuint32_t>(spa::kTileRows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  if (encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return SPA_ERR_CUDA;
   return SPA_OK;
+}
+int encode_bf16_rows(CUtensorMap* map, const void* base, int inner, int N, int BH) {
+  return encode_rows_map(map, base, inner, N, BH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2);
 }
 
 // Stage 1: projection of q and k into the workspace.
@@ -161,8 +167,8 @@ int run_prepare(const void* q, const void* k, const void* P, int B, int H, int N
   pp.use_tc = 1;
   if (spa::project_tc_eligible(pp)) {
     int st;
-    if ((st = encode_rows_map(&pp.xmap[0], q, d, N, B * H))) return st;
-    if ((st = encode_rows_map(&pp.xmap[1], k, d, N, B * H))) return st;
+    if ((st = encode_bf16_rows(&pp.xmap[0], q, d, N, B * H))) return st;
+    if ((st = encode_bf16_rows(&pp.xmap[1], k, d, N, B * H))) return st;
     if ((st = device_error_ptr(&pp.err))) return st;
   }
   return cuda_status(spa::launch_project(pp, stream));
@@ -190,7 +196,9 @@ int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int
   }
   int st;
   spa::AttnTcParams ap{};
-  if ((st = encode_rows_map(&ap.vmap, v, dv, N, BH))) return st;
+  if ((st = encode_bf16_rows(&ap.vmap, v, dv, N, BH))) return st;
+  if ((st = encode_rows_map(&ap.omap, out, dv, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)))
+    return st;
   int* err = nullptr;
   if ((st = device_error_ptr(&err))) return st;
   ap.Qs = reinterpret_cast<const uint16_t*>(w + L.qs);
