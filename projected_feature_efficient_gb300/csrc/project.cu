@@ -4,9 +4,11 @@
 //
 // Two kernels compute it:
 //   project_tc_kernel  (bf16 inputs, d a multiple of 8, score-operand output):
-//       a 128-row tile of X arrives by TMA (128-byte swizzle, K-major), P_h^T
-//       is written into shared memory in the tensor cores' interleaved layout,
-//       and one tcgen05 GEMM of shape 128 x m x d accumulates Xp in TMEM (fp32).
+//       persistent CTAs, each over a contiguous range of 128-row tiles; X
+//       tiles arrive by TMA (128-byte swizzle, K-major) two ahead, P_h^T is
+//       written into shared memory in the tensor cores' interleaved layout
+//       when the head changes, and one tcgen05 GEMM of shape 128 x m x d per
+//       tile accumulates Xp in TMEM (fp32).
 //   project_kernel     (any d, fp32 or bf16 inputs, any output mode):
 //       SIMT fp32 FMA; thread r of a 128-thread CTA computes row r with P_h
 //       staged in shared memory.
@@ -175,76 +177,116 @@ __global__ void __launch_bounds__(128) project_kernel(const ProjParams p) {
 // ------------------------------------------------------------------ tcgen05 kernel
 constexpr uint64_t kProjWaitNs = 2000000000ull;
 
-template <int MP>
+template <int MP, int DCH>
 struct ProjTcPlan {
   static constexpr int kCols = MP < 32 ? 32 : MP;   // TMEM columns (power of 2 >= 32)
   static constexpr int kXBox = kTileRows * 64 * 2;  // one 64-column TMA box: 16 KB
+  static constexpr int kXTile = DCH * kXBox;        // one 128-row X tile
+  static constexpr int kB = 2 * kXTile;             // two X tiles in flight, then P_h^T
+  static constexpr int kBytes = kB + MP * DCH * 64 * 2 + 1024;
 };
 
-// X tile (128 rows x d, bf16) by TMA into DCH boxes of [128][64] with 128-byte
-// swizzle; B = P_h^T (MP x 64*DCH) in the interleaved K-major layout.
+// Persistent projection: CTA c takes the contiguous range of units
+// [c*U/G, (c+1)*U/G) of the list (tensor, head, 128-row tile), so every CTA
+// gets the same number of tiles to within one and re-stages P_h only when
+// the head changes.  X tiles (128 rows x d, bf16) arrive by TMA, two ahead,
+// into DCH boxes of [128][64] with 128-byte swizzle; B = P_h^T (MP x 64*DCH)
+// sits in shared memory in the interleaved K-major layout; one tcgen05 GEMM of
+// shape 128 x MP x d per tile accumulates in TMEM, and all 128 threads run
+// the epilogue while the next tiles load.
 template <int MP, int DCH, ProjOut MODE>
 __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
                                                          const __grid_constant__ CUtensorMap xq,
                                                          const __grid_constant__ CUtensorMap xk) {
   using namespace ptx;
-  using Plan = ProjTcPlan<MP>;
+  using Plan = ProjTcPlan<MP, DCH>;
   constexpr int DP = DCH * 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sX = smem;  // DCH * 16 KB
-  uint16_t* sB = reinterpret_cast<uint16_t*>(smem + DCH * Plan::kXBox);  // MP * DP
-  __shared__ uint64_t bar_load, bar_mma;
+  uint16_t* sB = reinterpret_cast<uint16_t*>(smem + Plan::kB);  // MP * DP
+  __shared__ uint64_t bar_x[2], bar_mma;
   __shared__ uint32_t tmem_base_sh;
   __shared__ float red[4];
-  const int tile = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const CUtensorMap* xmap = which == 0 ? &xq : &xk;
+  const long long U = static_cast<long long>(p.nx) * p.BH * p.NT;
+  const long long G = gridDim.x;
+  const long long u0 = blockIdx.x * U / G, u1 = (blockIdx.x + 1) * U / G;
+
+  // unit -> (tensor, head, tile)
+  auto unit_which = [&](long long u) { return static_cast<int>(u / (static_cast<long long>(p.BH) * p.NT)); };
+  auto unit_bh = [&](long long u) { return static_cast<int>((u / p.NT) % p.BH); };
+  auto unit_tile = [&](long long u) { return static_cast<int>(u % p.NT); };
+  int issued = 0, commits = 0;  // thread 0: X copies started, GEMM commits
+  auto load = [&](long long u, int slot) {  // thread 0 only
+    ++issued;
+    const CUtensorMap* xmap = unit_which(u) == 0 ? &xq : &xk;
+    uint8_t* dst = smem + slot * Plan::kXTile;
+    mbar_arrive_expect_tx(&bar_x[slot], Plan::kXTile);
+#pragma unroll
+    for (int c = 0; c < DCH; ++c)
+      tma_load_3d(dst + c * Plan::kXBox, xmap, c * 64, unit_tile(u) * kTileRows, unit_bh(u),
+                  &bar_x[slot]);
+  };
 
   if (warp == 0) {
     tmem_alloc(&tmem_base_sh, Plan::kCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&bar_load, 1);
+    mbar_init(&bar_x[0], 1);
+    mbar_init(&bar_x[1], 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar_load, DCH * Plan::kXBox);
-#pragma unroll
-    for (int c = 0; c < DCH; ++c)
-      tma_load_3d(sX + c * Plan::kXBox, xmap, c * 64, tile * kTileRows, bh, &bar_load);
+    if (u0 < u1) load(u0, 0);
+    if (u0 + 1 < u1) load(u0 + 1, 1);
   }
-  // B operand: element (n, k) = P_h[k][n] at ((k/8)*(MP/8) + n/8)*64 + (n%8)*8 + k%8
-  const __nv_bfloat16* P =
-      static_cast<const __nv_bfloat16*>(p.P) + static_cast<size_t>(bh % p.H) * p.d * p.m;
-  for (int i = tid; i < MP * DP; i += 128) {
-    const int k = i / MP, n = i % MP;
-    const uint16_t v = k < p.d ? __bfloat16_as_ushort(P[k * p.m + n]) : uint16_t(0);
-    sB[((k >> 3) * (MP / 8) + (n >> 3)) * 64 + (n & 7) * 8 + (k & 7)] = v;
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base_sh;
 
-  bool ok = __syncthreads_and(mbar_wait(&bar_load, 0, kProjWaitNs));
-  if (ok && tid == 0) {
-    constexpr uint32_t idesc = idesc_f16(128, MP, kFmtBF16, 0, 0);
-    tc_fence_after();
-#pragma unroll
-    for (int s = 0; s < DP / 16; ++s) {
-      const uint64_t ad = smem_desc(smem_u32(sX) + (s >> 2) * Plan::kXBox + (s & 3) * 32, 16,
-                                    1024, kLayoutSwizzle128);
-      const uint64_t bd = smem_desc(smem_u32(sB) + s * 2 * (MP / 8) * 128, (MP / 8) * 128, 128,
-                                    kLayoutInterleave);
-      mma_ss(tb, ad, bd, idesc, s > 0);
+  bool ok = true;
+  int staged_h = -1;
+  for (long long u = u0; ok && u < u1; ++u) {
+    const int i = static_cast<int>(u - u0), slot = i & 1;
+    const int which = unit_which(u), bh = unit_bh(u), tile = unit_tile(u);
+    const int h = bh % p.H;
+    if (h != staged_h) {
+      // B operand: element (n, k) = P_h[k][n] at ((k/8)*(MP/8) + n/8)*64 + (n%8)*8 + k%8.
+      // The previous GEMM has completed (waited below), so sB is free.
+      const __nv_bfloat16* P =
+          static_cast<const __nv_bfloat16*>(p.P) + static_cast<size_t>(h) * p.d * p.m;
+      for (int e = tid; e < MP * DP; e += 128) {
+        const int k = e / MP, n = e % MP;
+        const uint16_t v = k < p.d ? __bfloat16_as_ushort(P[k * p.m + n]) : uint16_t(0);
+        sB[((k >> 3) * (MP / 8) + (n >> 3)) * 64 + (n & 7) * 8 + (k & 7)] = v;
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      staged_h = h;
     }
-    mma_commit(&bar_mma);
-  }
-  if (ok) ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kProjWaitNs));
-  if (ok) {
+    ok = __syncthreads_and(mbar_wait(&bar_x[slot], (i >> 1) & 1, kProjWaitNs));
+    if (!ok) break;
+    if (tid == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, MP, kFmtBF16, 0, 0);
+      const uint32_t sx = smem_u32(smem + slot * Plan::kXTile);
+      tc_fence_after();
+#pragma unroll
+      for (int st = 0; st < DP / 16; ++st) {
+        const uint64_t ad = smem_desc(sx + (st >> 2) * Plan::kXBox + (st & 3) * 32, 16, 1024,
+                                      kLayoutSwizzle128);
+        const uint64_t bd = smem_desc(smem_u32(sB) + st * 2 * (MP / 8) * 128, (MP / 8) * 128, 128,
+                                      kLayoutInterleave);
+        mma_ss(tb, ad, bd, idesc, st > 0);
+      }
+      mma_commit(&bar_mma);
+      ++commits;
+    }
+    ok = __syncthreads_and(mbar_wait(&bar_mma, i & 1, kProjWaitNs));
+    if (!ok) break;
+    // the GEMM has read X slot `slot`: refill it two tiles ahead
+    if (tid == 0 && u + 2 < u1) load(u + 2, slot);
     tc_fence_after();
     float acc[MP];
 #pragma unroll
@@ -253,16 +295,24 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
       tmem_ld16(tb + (static_cast<uint32_t>(warp * 32) << 16) + c, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(r[i]);
+      for (int q = 0; q < 16; ++q) acc[c + q] = __uint_as_float(r[q]);
     }
+    // every thread's accumulator is read before the next GEMM overwrites it
+    tc_fence_before();
+    __syncthreads();
     store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red);
-  } else {
-    if (tid == 0) atomicExch(p.err, 1);
-    // the TMA copy or the MMA may still be in flight: let it finish before exit
-    mbar_wait(&bar_load, 0, kProjWaitNs);
-    if (tid == 0) mma_commit(&bar_mma);
-    mbar_wait(&bar_mma, 0, kProjWaitNs);
   }
+  if (tid == 0 && !ok) {
+    atomicExch(p.err, 1);
+    // a GEMM may still be in flight: let it finish before TMEM is released
+    mma_commit(&bar_mma);
+    mbar_wait(&bar_mma, commits & 1, kProjWaitNs);
+  }
+  // every X copy started lands before the CTA's memory is released (all of
+  // them already have unless a wait gave up): the last copy into each slot
+  if (tid == 0)
+    for (int i = max(0, issued - 2); i < issued; ++i)
+      mbar_wait(&bar_x[i & 1], (i >> 1) & 1, kProjWaitNs);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, Plan::kCols);
@@ -284,17 +334,23 @@ cudaError_t launch_one(const ProjParams& p, cudaStream_t stream) {
 
 template <int MP, int DCH, ProjOut MODE>
 cudaError_t launch_tc_one(const ProjParams& p, cudaStream_t stream) {
-  using Plan = ProjTcPlan<MP>;
+  using Plan = ProjTcPlan<MP, DCH>;
   auto kern = project_tc_kernel<MP, DCH, MODE>;
-  int smem = DCH * Plan::kXBox + MP * DCH * 64 * 2 + 1024;
-  // never more CTAs per SM than their TMEM allocations fit in 512 columns
-  const int max_ctas = 512 / Plan::kCols;
-  const int min_smem = 233472 / (max_ctas + 1) + 1;  // 228 KB of shared memory per SM
-  if (smem < min_smem) smem = min_smem;
+  const int smem = Plan::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.NT, p.BH, p.nx);
-  kern<<<grid, 128, smem, stream>>>(p, p.xmap[0], p.xmap[1]);
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, smem)) != cudaSuccess)
+    return e;
+  // never more CTAs per SM than their TMEM allocations fit in 512 columns
+  per_sm = max(1, min(per_sm, 512 / Plan::kCols));
+  const long long units = static_cast<long long>(p.nx) * p.BH * p.NT;
+  const long long grid = min(units, static_cast<long long>(sms) * per_sm);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<unsigned>(grid), 128, smem, stream>>>(p, p.xmap[0], p.xmap[1]);
   return cudaGetLastError();
 }
 
