@@ -93,6 +93,12 @@ SMALL = [
     (2, 2, 777, 64, 128, 64, False),
     (1, 1, 1281, 128, 32, 128, False),
     (1, 2, 1281, 128, 64, 128, True),
+    # more work items than SMs: each persistent CTA walks several query-tile
+    # pairs of different heads, among them pairs without a second tile (odd
+    # tile count), and projection ranges that cross heads and the q/k boundary
+    (3, 60, 300, 64, 32, 64, True),
+    (2, 90, 300, 128, 64, 128, False),
+    (2, 80, 260, 64, 16, 64, True),
 ]
 
 
