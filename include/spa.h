@@ -130,8 +130,13 @@ int spa_attention_apply(const void *v, float *out, int B, int H, int N, int d, i
 /*
  * spa_attention_fwd_host -- end-to-end form on HOST buffers: copies q, k, v, P
  * to the device, runs the forward, copies out back, and synchronises `stream`
- * before returning, so `out` is valid on return.  Device buffers and the
- * workspace are taken with cudaMallocAsync and released before return.
+ * before returning, so `out` is valid on return.  Heads are independent, so
+ * the (batch, head) range is cut into chunks of whole heads (at least about
+ * 32 MB of traffic each, at most 16 chunks) that run on three internal
+ * streams forked from and joined back into `stream`: chunk c+1 is copied in
+ * and chunk c-1 copied out while chunk c computes.  The result is bit for bit
+ * that of spa_attention_fwd.  Device buffers and workspace for three chunks
+ * are taken with cudaMallocAsync on `stream` and released before return.
  * Page-locked host buffers give asynchronous, full-bandwidth copies; pageable
  * ones work but copy synchronously.  Same shapes and dtypes as
  * spa_attention_fwd.

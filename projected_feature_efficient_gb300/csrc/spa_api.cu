@@ -235,6 +235,93 @@ int check_forward_ptrs(const void* q, const void* k, const void* v, const void* 
 
 }  // namespace
 
+namespace {
+
+// Host-buffer forward, pipelined over chunks of whole heads of one batch
+// entry: chunk c is copied in, projected, attended and copied out on stream
+// slot c % kHostSlots, so the copy engines bring chunk c+1 in and take chunk
+// c-1 out while chunk c computes.  Heads are independent, and a chunk of heads
+// [h0, h0+n) of batch entry b is the problem (B=1, H=n) on the matching slices
+// of q, k, v, out and P.
+constexpr int kHostSlots = 3;
+constexpr size_t kHostChunkBytes = size_t(32) << 20;  // aim for at least this per chunk
+constexpr int kHostMaxChunks = 16;
+
+int host_forward(const char* q, const char* k, const char* v, const char* P, float* out, int B,
+                 int H, int N, int d, int m, int dv, int causal, int dtype, cudaStream_t stream) {
+  const size_t es = dtype == SPA_BF16 ? 2 : 4;
+  const size_t head_in = static_cast<size_t>(N) * (2 * d + dv) * es;
+  const size_t head_out = static_cast<size_t>(N) * dv * sizeof(float);
+  const size_t total_heads = static_cast<size_t>(B) * H;
+  const size_t want = (total_heads * (head_in + head_out)) / kHostChunkBytes;
+  const size_t nchunks = want < 1 ? 1 : (want > kHostMaxChunks ? kHostMaxChunks : want);
+  size_t per = (total_heads + nchunks - 1) / nchunks;
+  const int nh = static_cast<int>(per < 1 ? 1 : (per > static_cast<size_t>(H) ? H : per));
+
+  // one slot: q, k, v, P slices, out slice and the workspace for nh heads
+  const size_t nq = static_cast<size_t>(nh) * N * d * es, nv = static_cast<size_t>(nh) * N * dv * es;
+  const size_t np = static_cast<size_t>(nh) * d * m * es, no = static_cast<size_t>(nh) * N * dv * 4;
+  const size_t oq = 0, ok = align256(oq + nq), ov = align256(ok + nq), op = align256(ov + nv),
+               oo = align256(op + np), ow = align256(oo + no);
+  const size_t slot_bytes = align256(ow + make_layout(1, nh, N, m, dtype).total);
+
+  cudaStream_t ss[kHostSlots] = {};
+  cudaEvent_t ev_begin = nullptr, ev_end[kHostSlots] = {};
+  char* dbuf = nullptr;
+  int st = SPA_OK;
+  auto fail = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == SPA_OK) st = SPA_ERR_CUDA;
+    return e != cudaSuccess;
+  };
+  if (cudaMallocAsync(reinterpret_cast<void**>(&dbuf), kHostSlots * slot_bytes, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  bool ready = !fail(cudaEventCreateWithFlags(&ev_begin, cudaEventDisableTiming)) &&
+               !fail(cudaEventRecord(ev_begin, stream));
+  for (int j = 0; ready && j < kHostSlots; ++j)
+    ready = !fail(cudaStreamCreateWithFlags(&ss[j], cudaStreamNonBlocking)) &&
+            !fail(cudaEventCreateWithFlags(&ev_end[j], cudaEventDisableTiming)) &&
+            !fail(cudaStreamWaitEvent(ss[j], ev_begin, 0));
+  int c = 0;
+  for (int b = 0; ready && st == SPA_OK && b < B; ++b) {
+    for (int h0 = 0; st == SPA_OK && h0 < H; h0 += nh, ++c) {
+      const int n = H - h0 < nh ? H - h0 : nh;
+      cudaStream_t sj = ss[c % kHostSlots];
+      char* sb = dbuf + (c % kHostSlots) * slot_bytes;
+      const size_t head0 = static_cast<size_t>(b) * H + h0;
+      const size_t cq = static_cast<size_t>(n) * N * d * es, cv = static_cast<size_t>(n) * N * dv * es;
+      if (fail(cudaMemcpyAsync(sb + oq, q + head0 * N * d * es, cq, cudaMemcpyHostToDevice, sj)) ||
+          fail(cudaMemcpyAsync(sb + ok, k + head0 * N * d * es, cq, cudaMemcpyHostToDevice, sj)) ||
+          fail(cudaMemcpyAsync(sb + ov, v + head0 * N * dv * es, cv, cudaMemcpyHostToDevice, sj)) ||
+          fail(cudaMemcpyAsync(sb + op, P + static_cast<size_t>(h0) * d * m * es,
+                               static_cast<size_t>(n) * d * m * es, cudaMemcpyHostToDevice, sj)))
+        break;
+      st = run_forward(sb + oq, sb + ok, sb + ov, sb + op, reinterpret_cast<float*>(sb + oo), 1, n,
+                       N, d, m, dv, causal, dtype, sb + ow, sj);
+      if (st) break;
+      if (fail(cudaMemcpyAsync(out + head0 * N * dv, sb + oo, static_cast<size_t>(n) * N * dv * 4,
+                               cudaMemcpyDeviceToHost, sj)))
+        break;
+    }
+  }
+  // join every slot back into the caller's stream, release, and wait
+  for (int j = 0; j < kHostSlots; ++j)
+    if (ss[j] && ev_end[j] && !fail(cudaEventRecord(ev_end[j], ss[j])))
+      fail(cudaStreamWaitEvent(stream, ev_end[j], 0));
+  fail(cudaFreeAsync(dbuf, stream));
+  fail(cudaStreamSynchronize(stream));
+  for (int j = 0; j < kHostSlots; ++j) {
+    if (ev_end[j]) cudaEventDestroy(ev_end[j]);
+    if (ss[j]) cudaStreamDestroy(ss[j]);
+  }
+  if (ev_begin) cudaEventDestroy(ev_begin);
+  return st;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* spa_status_str(int status) {
@@ -361,33 +448,9 @@ int spa_attention_fwd_host(const void* q, const void* k, const void* v, const vo
   if (st == kEmpty) return SPA_OK;
   if (st) return st;
   if (!q || !k || !v || !P || !out) return SPA_ERR_NULL;
-  const size_t es = dtype == SPA_BF16 ? 2 : 4;
-  const size_t BHN = static_cast<size_t>(B) * H * N;
-  const size_t nq = BHN * d * es, nv = BHN * d_v * es, np = static_cast<size_t>(H) * d * m * es;
-  const size_t no = BHN * d_v * sizeof(float);
-  const size_t oq = 0, ok = align256(oq + nq), ov = align256(ok + nq), op = align256(ov + nv),
-               oo = align256(op + np), ow = align256(oo + no);
-  const size_t total = ow + make_layout(B, H, N, m, dtype).total;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* dbuf = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&dbuf), total, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
-  }
-  cudaError_t e = cudaMemcpyAsync(dbuf + oq, q, nq, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + ok, k, nq, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + ov, v, nv, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + op, P, np, cudaMemcpyHostToDevice, s);
-  st = cuda_status(e);
-  if (!st)
-    st = run_forward(dbuf + oq, dbuf + ok, dbuf + ov, dbuf + op, reinterpret_cast<float*>(dbuf + oo),
-                     B, H, N, d, m, d_v, causal, dtype, dbuf + ow, s);
-  if (!st) st = cuda_status(cudaMemcpyAsync(out, dbuf + oo, no, cudaMemcpyDeviceToHost, s));
-  const cudaError_t fe = cudaFreeAsync(dbuf, s);
-  const cudaError_t se = cudaStreamSynchronize(s);
-  if (st) return st;
-  if (fe != cudaSuccess || se != cudaSuccess) return SPA_ERR_CUDA;
-  return SPA_OK;
+  return host_forward(static_cast<const char*>(q), static_cast<const char*>(k),
+                      static_cast<const char*>(v), static_cast<const char*>(P), out, B, H, N, d, m,
+                      d_v, causal, dtype, static_cast<cudaStream_t>(stream));
 }
 
 int spa_device_error(int* code) {

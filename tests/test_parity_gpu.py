@@ -168,6 +168,25 @@ def test_workspace_and_host_forms_agree_bitwise():
     assert torch.equal(a, pkg.spa_attention_fwd(dq, dk, dv_, dP, causal=True))
 
 
+@pytest.mark.parametrize("B,H,causal", [(2, 8, True), (1, 7, False)])
+def test_host_form_chunked_matches_device_bitwise(B, H, causal):
+    """Large enough that the host form copies and computes in chunks of heads
+    (several chunks per stream slot, a short last chunk when H does not
+    divide): every head is computed alone, so the result is bit for bit the
+    device form's."""
+    pkg = spa()
+    w = si.WORKLOADS["C2"].scaled(B=B, H=H, N=16384, causal=causal)
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn((B, H, w.N, w.d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H, w.N, w.d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, w.N, w.dv), generator=g).to(torch.bfloat16)
+    P = (torch.randn((H, w.d, w.m), generator=g) / w.m ** 0.5).to(torch.bfloat16)
+    a = pkg.spa_attention_fwd(q.cuda(), k.cuda(), v.cuda(), P.cuda(), causal=causal).cpu()
+    c = pkg.spa_attention_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(),
+                                   P.pin_memory(), causal=causal)
+    assert torch.equal(a, c)
+
+
 def test_rows_sum_to_one_through_constant_values():
     """V = 1 gives O = 1 exactly up to the bf16 rounding of the probabilities."""
     w = si.WORKLOADS["C3"].scaled(B=1, H=2, N=513, causal=True)
