@@ -339,12 +339,25 @@ cudaError_t launch_tc_one(const ProjParams& p, cudaStream_t stream) {
   const int smem = Plan::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // the whole unified L1 as shared memory, so that several CTAs are resident
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, per_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, smem)) != cudaSuccess)
     return e;
+  // The occupancy query may assume the default L1 / shared split; with the
+  // whole carveout as shared memory, this many CTAs fit by shared memory.
+  int sm_smem = 0, reserved = 0;
+  if ((e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+          cudaSuccess)
+    return e;
+  per_sm = max(per_sm, sm_smem / (smem + reserved));
   // never more CTAs per SM than their TMEM allocations fit in 512 columns
   per_sm = max(1, min(per_sm, 512 / Plan::kCols));
   const long long units = static_cast<long long>(p.nx) * p.BH * p.NT;
