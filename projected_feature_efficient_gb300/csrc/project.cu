@@ -254,13 +254,33 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
     const int h = bh % p.H;
     if (h != staged_h) {
       // B operand: element (n, k) = P_h[k][n] at ((k/8)*(MP/8) + n/8)*64 + (n%8)*8 + k%8.
-      // The previous GEMM has completed (waited below), so sB is free.
-      const __nv_bfloat16* P =
-          static_cast<const __nv_bfloat16*>(p.P) + static_cast<size_t>(h) * p.d * p.m;
-      for (int e = tid; e < MP * DP; e += 128) {
-        const int k = e / MP, n = e % MP;
-        const uint16_t v = k < p.d ? __bfloat16_as_ushort(P[k * p.m + n]) : uint16_t(0);
-        sB[((k >> 3) * (MP / 8) + (n >> 3)) * 64 + (n & 7) * 8 + (k & 7)] = v;
+      // The previous GEMM has completed (waited below), so sB is free.  Each
+      // thread reads 8 consecutive n of one row k of P_h (16 bytes; m == MP is
+      // a multiple of 8 and P is 16-byte aligned) and all its reads are issued
+      // before the first store, so the L2 latency is paid about once.
+      const uint4* P = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.P) +
+                                                      static_cast<size_t>(h) * p.d * MP);
+      constexpr int kVec = MP * DP / 8;  // 16-byte pieces of P_h^T (zero rows past d)
+      constexpr int kPer = (kVec + 127) / 128;
+      uint4 pv[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = tid + i * 128, k = e / (MP / 8), n0 = (e % (MP / 8)) * 8;
+        pv[i] = (e < kVec && k < p.d) ? __ldg(P + (static_cast<size_t>(k) * MP + n0) / 8)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = tid + i * 128, k = e / (MP / 8), n0 = (e % (MP / 8)) * 8;
+        if (e < kVec) {
+          uint16_t* dst = sB + ((k >> 3) * (MP / 8) + (n0 >> 3)) * 64 + (k & 7);
+          const uint32_t w[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            dst[(2 * q) * 8] = static_cast<uint16_t>(w[q] & 0xFFFFu);
+            dst[(2 * q + 1) * 8] = static_cast<uint16_t>(w[q] >> 16);
+          }
+        }
       }
       fence_proxy_async_smem();
       __syncthreads();
