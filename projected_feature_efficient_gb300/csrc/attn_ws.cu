@@ -144,6 +144,102 @@ __device__ __forceinline__ int item_index(int k, int items) {
   return w < items ? w : -1;
 }
 
+// ---------------------------------------------------------------- loader
+// The loader role (one thread): per item the Qp tiles of its query-tile pair,
+// then the item's key tiles through the ring of Plan::kStages slots, each slot
+// a Kp tile (one bulk copy) and a V tile (TMA, 128-byte swizzle) completing on
+// one barrier.  Every item starts at slot 0 and every slot keeps its own phase
+// bits, so the issuer's slot numbers stay compile-time constants.  Before it
+// returns, every copy it started has landed.
+template <class Plan, int KD, int DV>
+__device__ __forceinline__ void run_loader(const AttnTcParams& p, const CUtensorMap* vmap,
+                                           uint8_t* smem, Bars& bars, volatile int* abort_sh,
+                                           int items) {
+  constexpr int S = Plan::kStages;
+  constexpr int kTileElems = kTileRows * KD;
+  prefetch_tmap(vmap);
+  uint32_t used = 0, emph = 0, armph = 0;  // per ring slot: used before, kv_empty / kv_full phase bits
+  int qarmed = 0;                          // Q loads started
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int w = item_index(k, items);
+    if (w < 0) break;
+    const Item it = decode_item(p, w);
+    if (k > 0 && !(ok = wait_or_abort(&bars.q_empty, (k - 1) & 1, abort_sh, p.err))) break;
+    const uint16_t* Qs = p.Qs + (static_cast<size_t>(it.bh) * p.NT + it.qt0) * kTileElems;
+    const uint16_t* Ks = p.Ks + static_cast<size_t>(it.bh) * p.NT * kTileElems;
+    mbar_arrive_expect_tx(&bars.q_full, (it.nkv1 > 0 ? 2 : 1) * Plan::kQBytes);
+    bulk_g2s(smem + Plan::kQ, Qs, Plan::kQBytes, &bars.q_full);
+    if (it.nkv1 > 0)
+      bulk_g2s(smem + Plan::kQ + Plan::kQBytes, Qs + kTileElems, Plan::kQBytes, &bars.q_full);
+    qarmed = k + 1;
+    for (int j = 0; j < it.nkv; ++j) {
+      const int slot = j % S;
+      const uint32_t bit = 1u << slot;
+      if (used & bit) {
+        if (!(ok = wait_or_abort(&bars.kv_empty[slot], (emph & bit) ? 1u : 0u, abort_sh, p.err)))
+          break;
+        emph ^= bit;
+      }
+      used |= bit;
+      mbar_arrive_expect_tx(&bars.kv_full[slot], Plan::kKBytes + Plan::kVBytes);
+      bulk_g2s(smem + Plan::kK + slot * Plan::kKBytes, Ks + static_cast<size_t>(j) * kTileElems,
+               Plan::kKBytes, &bars.kv_full[slot]);
+      uint8_t* vdst = smem + Plan::kV + slot * Plan::kVBytes;
+#pragma unroll
+      for (int h = 0; h < DV / 64; ++h)
+        tma_load_3d(vdst + h * 16384, vmap, h * 64, j * kTileRows, it.bh, &bars.kv_full[slot]);
+      armph ^= bit;
+    }
+  }
+  // every copy this thread started lands before the CTA's memory is released
+  // (all of them already have, unless some role gave up)
+  if (qarmed > 0) mbar_wait(&bars.q_full, (qarmed - 1) & 1, kLimitNs);
+  for (int s = 0; s < S; ++s)
+    if (used & (1u << s)) mbar_wait(&bars.kv_full[s], ((armph >> s) & 1u) ^ 1u, kLimitNs);
+}
+
+// ---------------------------------------------------------------- output
+// One softmax warpgroup writes its finished O_t / l (fp32) for query tile qt:
+// DV/32 boxes of 128 rows x 128 B, staged in the 128-byte swizzle of the
+// output tensor map (16-byte chunk q of row r sits at chunk q ^ (r % 8), which
+// also spreads a warp's stores over all banks) through kBuffers box buffers
+// at `stage`, each written out by a TMA tile store that clips rows past N.
+// The warps arrive on o_empty once their last read of O_t is done.
+template <int DV, int kBuffers>
+__device__ __forceinline__ void write_out_tile(uint32_t tO, uint32_t stage, int r, int lane,
+                                               float inv, const CUtensorMap* omap, int qt, int bh,
+                                               uint32_t bar_id, uint64_t* o_empty) {
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+  for (int b = 0; b < DV / 32; ++b) {
+    uint32_t v[32];
+    tmem_ld32(tO + b * 32, v);
+    tmem_wait_ld();
+    if (b == DV / 32 - 1) {  // O_t is read out: the next PV_t(0) may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+    }
+    const uint32_t box = stage + (b % kBuffers) * kBoxBytes;
+    if (r == 0) bulk_wait_group_read<kBuffers - 1>();  // this buffer's last store has read it
+    named_bar_sync(bar_id, 128);
+    const uint32_t rb = box + r * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(rb + ((q ^ sw) << 4), __float_as_uint(__uint_as_float(v[4 * q]) * inv),
+                   __float_as_uint(__uint_as_float(v[4 * q + 1]) * inv),
+                   __float_as_uint(__uint_as_float(v[4 * q + 2]) * inv),
+                   __float_as_uint(__uint_as_float(v[4 * q + 3]) * inv));
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, 128);
+    if (r == 0) {
+      tma_store_3d(omap, box, b * 32, qt * kTileRows, bh);
+      bulk_commit_group();
+    }
+  }
+}
+
 template <int KD, int DV, bool F16OPS>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_ws_kernel(const AttnTcParams p, const __grid_constant__ CUtensorMap vmap,
@@ -185,54 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base_sh;
-  constexpr int kTileElems = kTileRows * KD;
   if (warp >= 8) {
    setmaxnreg_dec<RegSplit<KD>::kControl>();  // the whole control warpgroup
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
-    if (lane == 0) {
-      prefetch_tmap(&vmap);
-      uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
-      uint32_t used = 0, emph = 0, armph = 0;  // per ring slot: used before, kv_empty / kv_full phase bits
-      int qarmed = 0;                          // Q loads started
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int w = item_index(k, items);
-        if (w < 0) break;
-        const Item it = decode_item(p, w);
-        if (k > 0 && !(ok = wait_or_abort(&bars.q_empty, (k - 1) & 1, &abort_sh, p.err))) break;
-        const uint16_t* Qs = p.Qs + (static_cast<size_t>(it.bh) * p.NT + it.qt0) * kTileElems;
-        const uint16_t* Ks = p.Ks + static_cast<size_t>(it.bh) * p.NT * kTileElems;
-        mbar_arrive_expect_tx(&bars.q_full, (it.nkv1 > 0 ? 2 : 1) * Plan::kQBytes);
-        bulk_g2s(smem + Plan::kQ, Qs, Plan::kQBytes, &bars.q_full);
-        if (it.nkv1 > 0)
-          bulk_g2s(smem + Plan::kQ + Plan::kQBytes, Qs + kTileElems, Plan::kQBytes, &bars.q_full);
-        qarmed = k + 1;
-        for (int j = 0; j < it.nkv; ++j) {
-          const int slot = j % S;
-          const uint32_t bit = 1u << slot;
-          if (used & bit) {
-            if (!(ok = wait_or_abort(&bars.kv_empty[slot], (emph & bit) ? 1u : 0u, &abort_sh, p.err)))
-              break;
-            emph ^= bit;
-          }
-          used |= bit;
-          mbar_arrive_expect_tx(&bars.kv_full[slot], Plan::kKBytes + Plan::kVBytes);
-          bulk_g2s(smem + Plan::kK + slot * Plan::kKBytes, Ks + static_cast<size_t>(j) * kTileElems,
-                   Plan::kKBytes, &bars.kv_full[slot]);
-          uint8_t* vdst = smem + Plan::kV + slot * Plan::kVBytes;
-#pragma unroll
-          for (int h = 0; h < DV / 64; ++h)
-            tma_load_3d(vdst + h * 16384, &vmap, h * 64, j * kTileRows, it.bh, &bars.kv_full[slot]);
-          armph ^= bit;
-        }
-      }
-      // every copy this thread started lands before the CTA's memory is released
-      // (all of them already have, unless some role gave up)
-      if (qarmed > 0) mbar_wait(&bars.q_full, (qarmed - 1) & 1, kLimitNs);
-      for (int s = 0; s < S; ++s)
-        if (used & (1u << s)) mbar_wait(&bars.kv_full[s], ((armph >> s) & 1u) ^ 1u, kLimitNs);
-    }
+    if (lane == 0)
+      run_loader<Plan, KD, DV>(p, &vmap, smem_raw + (sbase - smem_u32(smem_raw)), bars, &abort_sh,
+                               items);
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -461,39 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv = 1.f / l_run;
-      // Staging: DV/32 boxes of 128 rows x 128 B, in the 128-byte swizzle of
-      // the output tensor map (16-byte chunk q of row r sits at chunk q ^ (r % 8),
-      // which also spreads a warp's stores over all banks), through
-      // kBoxesPerTile buffers of this tile.  The store clips rows past N.
-      const uint32_t stage = sbase + Plan::kStage + t * Plan::kBoxesPerTile * kBoxBytes;
-      const uint32_t sw = static_cast<uint32_t>(r & 7);
-#pragma unroll
-      for (int b = 0; b < DV / 32; ++b) {
-        uint32_t v[32];
-        tmem_ld32(tO + b * 32, v);
-        tmem_wait_ld();
-        if (b == DV / 32 - 1) {  // O_t is read out: the next PV_t(0) may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.o_empty[t]);
-        }
-        const uint32_t box = stage + (b % Plan::kBoxesPerTile) * kBoxBytes;
-        if (r == 0) bulk_wait_group_read<Plan::kBoxesPerTile - 1>();  // this buffer's last store has read it
-        named_bar_sync(bar_id, 128);
-        const uint32_t rb = box + r * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(rb + ((q ^ sw) << 4), __float_as_uint(__uint_as_float(v[4 * q]) * inv),
-                       __float_as_uint(__uint_as_float(v[4 * q + 1]) * inv),
-                       __float_as_uint(__uint_as_float(v[4 * q + 2]) * inv),
-                       __float_as_uint(__uint_as_float(v[4 * q + 3]) * inv));
-        fence_proxy_async_smem();
-        named_bar_sync(bar_id, 128);
-        if (r == 0) {
-          tma_store_3d(&omap, box, b * 32, qt * kTileRows, it.bh);
-          bulk_commit_group();
-        }
-      }
+      write_out_tile<DV, Plan::kBoxesPerTile>(
+          tO, sbase + Plan::kStage + t * Plan::kBoxesPerTile * kBoxBytes, r, lane, inv, &omap, qt,
+          it.bh, bar_id, &bars.o_empty[t]);
       ++ndone;
     }
     if (r == 0) bulk_wait_group_read<0>();  // the stores have read shared memory
@@ -514,10 +539,8 @@ int num_sms() {
   return n;
 }
 
-template <int KD, int DV, bool F16OPS>
-cudaError_t launch_ws(const AttnTcParams& p, cudaStream_t stream) {
-  using Plan = WsPlan<KD, DV>;
-  auto kern = attn_ws_kernel<KD, DV, F16OPS>;
+template <class Plan, class Kernel>
+cudaError_t launch_persistent(Kernel kern, const AttnTcParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Plan::kLaunch);
   if (e != cudaSuccess) return e;
@@ -528,6 +551,11 @@ cudaError_t launch_ws(const AttnTcParams& p, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   kern<<<grid, kThreads, Plan::kLaunch, stream>>>(p, p.vmap, p.omap);
   return cudaGetLastError();
+}
+
+template <int KD, int DV, bool F16OPS>
+cudaError_t launch_ws(const AttnTcParams& p, cudaStream_t stream) {
+  return launch_persistent<WsPlan<KD, DV>>(attn_ws_kernel<KD, DV, F16OPS>, p, stream);
 }
 
 template <int DV>
