@@ -169,6 +169,22 @@ int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const
                               int dtype, void *stream);
 
 /*
+ * spa_selftest_wait_timeout -- failure-detection self-test (the pages have no
+ * counterpart).  Runs one small bf16 forward (B=1 H=1 N=256 d=64 m=32 d_v=64,
+ * zero inputs, buffers taken and released with cudaMalloc/cudaFree on the
+ * current device, default stream) in which the attention kernel withholds one
+ * "scores ready" barrier arrival and limits every wait to limit_ms
+ * milliseconds (1..2000).  The waiting warps give up, every role of the
+ * kernel takes its abort path (drains its own copies and MMAs, frees tensor
+ * memory) and the kernel sets the device error word; nothing faults or hangs.
+ * The call synchronises the device, reads and clears the error word, and
+ * returns SPA_ERR_TIMEOUT when the timeout was reported (the expected
+ * outcome), SPA_OK when it was not, or another status if a call failed.  The
+ * device stays usable afterwards.
+ */
+int spa_selftest_wait_timeout(int limit_ms);
+
+/*
  * spa_device_error -- reads and clears the device error word of the current
  * device (synchronising it first).  *code receives 0 when no kernel gave up
  * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.

@@ -19,6 +19,7 @@ if not os.path.exists(lib_path):
 lib = ctypes.CDLL(lib_path)
 
 SPA_F32, SPA_BF16 = 0, 1
+SPA_OK, SPA_ERR_TIMEOUT = 0, 8  # spa_status values (include/spa.h)
 _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 
 lib.spa_status_str.argtypes = [_i]
@@ -43,6 +44,8 @@ lib.spa_attention_fwd_noalloc.argtypes = [_vp] * 5 + [_i] * 8 + [_vp]
 lib.spa_attention_fwd_noalloc.restype = _i
 lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
+lib.spa_selftest_wait_timeout.argtypes = [_i]
+lib.spa_selftest_wait_timeout.restype = _i
 
 
 class SpaError(RuntimeError):
@@ -177,6 +180,12 @@ def spa_attention_fwd_host(q, k, v, P, causal=False, out=None, stream=None):
                                       m, dv, int(bool(causal)), _dtype_code(q),
                                       _stream_ptr(stream)), "spa_attention_fwd_host")
     return out
+
+
+def selftest_wait_timeout(limit_ms: int = 50) -> int:
+    """Run the failure-detection self-test; returns the spa_status code
+    (SPA_ERR_TIMEOUT when the withheld barrier was detected, as expected)."""
+    return int(lib.spa_selftest_wait_timeout(int(limit_ms)))
 
 
 def device_error() -> int:

@@ -56,7 +56,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr uint64_t kLimitNs = 2000000000ull;
 constexpr int kThreads = 384;  // three warpgroups
 // Register split.  The block is launched with 384 x 168 = 64512 registers; the
 // control warpgroup (warps 8-11) gives up part of its share to the two
@@ -104,15 +103,22 @@ struct Bars {
   uint64_t drain;
 };
 
+// What a bounded wait needs: the CTA's abort flag, the device error word and
+// the time limit of one wait.
+struct WaitCtl {
+  volatile int* abort;
+  int* err;
+  uint64_t limit_ns;
+};
+
 // Bounded wait that also gives up once another role of the CTA has aborted.
 // The common case (phase already complete) costs one try_wait.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                              int* err) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;
-  if (*abort) return false;
-  if (mbar_wait(bar, parity, kLimitNs)) return true;
-  *abort = 1;
-  atomicExch(err, 1);
+  if (*ctl.abort) return false;
+  if (mbar_wait(bar, parity, ctl.limit_ns)) return true;
+  *ctl.abort = 1;
+  atomicExch(ctl.err, 1);
   return false;
 }
 
@@ -153,7 +159,7 @@ __device__ __forceinline__ int item_index(int k, int items) {
 // returns, every copy it started has landed.
 template <class Plan, int KD, int DV>
 __device__ __forceinline__ void run_loader(const AttnTcParams& p, const CUtensorMap* vmap,
-                                           uint8_t* smem, Bars& bars, volatile int* abort_sh,
+                                           uint8_t* smem, Bars& bars, const WaitCtl& ctl,
                                            int items) {
   constexpr int S = Plan::kStages;
   constexpr int kTileElems = kTileRows * KD;
@@ -165,7 +171,7 @@ __device__ __forceinline__ void run_loader(const AttnTcParams& p, const CUtensor
     const int w = item_index(k, items);
     if (w < 0) break;
     const Item it = decode_item(p, w);
-    if (k > 0 && !(ok = wait_or_abort(&bars.q_empty, (k - 1) & 1, abort_sh, p.err))) break;
+    if (k > 0 && !(ok = wait_or_abort(&bars.q_empty, (k - 1) & 1, ctl))) break;
     const uint16_t* Qs = p.Qs + (static_cast<size_t>(it.bh) * p.NT + it.qt0) * kTileElems;
     const uint16_t* Ks = p.Ks + static_cast<size_t>(it.bh) * p.NT * kTileElems;
     mbar_arrive_expect_tx(&bars.q_full, (it.nkv1 > 0 ? 2 : 1) * Plan::kQBytes);
@@ -177,7 +183,7 @@ __device__ __forceinline__ void run_loader(const AttnTcParams& p, const CUtensor
       const int slot = j % S;
       const uint32_t bit = 1u << slot;
       if (used & bit) {
-        if (!(ok = wait_or_abort(&bars.kv_empty[slot], (emph & bit) ? 1u : 0u, abort_sh, p.err)))
+        if (!(ok = wait_or_abort(&bars.kv_empty[slot], (emph & bit) ? 1u : 0u, ctl)))
           break;
         emph ^= bit;
       }
@@ -194,9 +200,9 @@ __device__ __forceinline__ void run_loader(const AttnTcParams& p, const CUtensor
   }
   // every copy this thread started lands before the CTA's memory is released
   // (all of them already have, unless some role gave up)
-  if (qarmed > 0) mbar_wait(&bars.q_full, (qarmed - 1) & 1, kLimitNs);
+  if (qarmed > 0) mbar_wait(&bars.q_full, (qarmed - 1) & 1, ctl.limit_ns);
   for (int s = 0; s < S; ++s)
-    if (used & (1u << s)) mbar_wait(&bars.kv_full[s], ((armph >> s) & 1u) ^ 1u, kLimitNs);
+    if (used & (1u << s)) mbar_wait(&bars.kv_full[s], ((armph >> s) & 1u) ^ 1u, ctl.limit_ns);
 }
 
 // ---------------------------------------------------------------- output
@@ -253,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = p.BH * ((p.NT + 1) >> 1);
+  const WaitCtl ctl{&abort_sh, p.err, p.limit_ns};
   // 1024-aligned operand area (128-byte swizzle atoms), as a shared-window address
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
 
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0)
-      run_loader<Plan, KD, DV>(p, &vmap, smem_raw + (sbase - smem_u32(smem_raw)), bars, &abort_sh,
+      run_loader<Plan, KD, DV>(p, &vmap, smem_raw + (sbase - smem_u32(smem_raw)), bars, ctl,
                                items);
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -297,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ0 = smem_desc(sbase + Plan::kQ, 2048, 128, kLayoutInterleave);
       const uint64_t dK = smem_desc(sbase + Plan::kK, 2048, 128, kLayoutInterleave);
       const uint64_t dV = smem_desc(sbase + Plan::kV, 16384, 1024, kLayoutSwizzle128);
+      bool first_s0 = true;
       auto issue_s = [&](int t, int slot) {  // S_t = Q_t K_slot^T, then signal the softmax
         const uint64_t a = dQ0 + static_cast<uint64_t>((t * Plan::kQBytes) >> 4);
         const uint64_t b = dK + static_cast<uint64_t>((slot * Plan::kKBytes) >> 4);
@@ -304,7 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < KD / 16; ++k)
           mma_ss(d, a + (k * 4096 >> 4), b + (k * 4096 >> 4), kIdescS, k > 0);
-        mma_commit(&bars.s_full[t]);
+        // a failure-detection test withholds the CTA's first "S0 ready": the
+        // softmax warps' wait for it runs out, and every role takes its abort path
+        if (!(p.inject_stall && t == 0 && first_s0)) mma_commit(&bars.s_full[t]);
+        if (t == 0) first_s0 = false;
       };
       auto issue_pv = [&](int t, int slot, uint32_t acc) {  // O_t += P_t V_slot
         const uint32_t a = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
@@ -323,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w < 0) break;
         const Item it = decode_item(p, w);
         const int nkv0 = it.nkv0, nkv1 = it.nkv1, nkv = it.nkv;
-        ok = wait_or_abort(&bars.q_full, k & 1, &abort_sh, p.err) &&
-             wait_or_abort(&bars.kv_full[0], fph & 1u, &abort_sh, p.err);
+        ok = wait_or_abort(&bars.q_full, k & 1, ctl) &&
+             wait_or_abort(&bars.kv_full[0], fph & 1u, ctl);
         if (!ok) break;
         fph ^= 1u;
         tc_fence_after();
@@ -333,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nkv == 1) mma_commit(&bars.q_empty);  // every score MMA of the item is issued
         // PV_t(0) overwrites O_t: the previous item's O_t must have been read
         // out.  Nothing else can be issued before PV0(0) anyway.
-        if (ndone0 > 0 && !(ok = wait_or_abort(&bars.o_empty[0], (ndone0 - 1) & 1, &abort_sh, p.err)))
+        if (ndone0 > 0 && !(ok = wait_or_abort(&bars.o_empty[0], (ndone0 - 1) & 1, ctl)))
           break;
         if (nkv1 > 0 && ndone1 > 0 &&
-            !(ok = wait_or_abort(&bars.o_empty[1], (ndone1 - 1) & 1, &abort_sh, p.err)))
+            !(ok = wait_or_abort(&bars.o_empty[1], (ndone1 - 1) & 1, ctl)))
           break;
         // key tiles in groups of S so that slot = u is a compile-time constant
         for (int j0 = 0; ok && j0 < nkv; j0 += S) {
@@ -347,19 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int un = (u + 1) % S;  // slot of key tile j+1
             const bool next = j + 1 < nkv;
             if (j < nkv0) {
-              if (!(ok = wait_or_abort(&bars.p_full[0], pph & 1u, &abort_sh, p.err))) break;
+              if (!(ok = wait_or_abort(&bars.p_full[0], pph & 1u, ctl))) break;
               pph ^= 1u;
               tc_fence_after();
               issue_pv(0, u, j > 0 ? 1u : 0u);
             }
             if (next) {
-              if (!(ok = wait_or_abort(&bars.kv_full[un], (fph >> un) & 1u, &abort_sh, p.err))) break;
+              if (!(ok = wait_or_abort(&bars.kv_full[un], (fph >> un) & 1u, ctl))) break;
               fph ^= 1u << un;
               tc_fence_after();
               if (j + 1 < nkv0) issue_s(0, un);
             }
             if (j < nkv1) {
-              if (!(ok = wait_or_abort(&bars.p_full[1], (pph >> 1) & 1u, &abort_sh, p.err))) break;
+              if (!(ok = wait_or_abort(&bars.p_full[1], (pph >> 1) & 1u, ctl))) break;
               pph ^= 2u;
               tc_fence_after();
               issue_pv(1, u, j > 0 ? 1u : 0u);
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nkv1 > 0) ++ndone1;
       }
       mma_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, kLimitNs);  // own MMAs in flight
+      mbar_wait(&bars.drain, 0, ctl.limit_ns);  // own MMAs in flight
     }
    }  // warps 10-11: no role
   } else {
@@ -411,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float km = __ldg(kmul + j);
         // warp-uniform outcome, so that the warp stays converged for the
         // .sync.aligned tensor-memory instructions below
-        if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars.s_full[t], sph, &abort_sh, p.err))))
+        if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars.s_full[t], sph, ctl))))
           break;
         sph ^= 1u;
         tc_fence_after();
@@ -512,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // barriers below as one; a thread that gave up has set abort_sh.
       __syncwarp();
       ok = named_bar_and(bar_id, 128,
-                         ok && wait_or_abort(&bars.o_final[t], ndone & 1, &abort_sh, p.err));
+                         ok && wait_or_abort(&bars.o_final[t], ndone & 1, ctl));
       if (!ok) break;
       tc_fence_after();
       const float inv = 1.f / l_run;

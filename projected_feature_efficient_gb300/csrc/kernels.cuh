@@ -50,6 +50,8 @@ struct AttnTcParams {
   int* err;              // device error word
   int BH, N, NT, KD, dv, causal;
   int f16_ops;           // 1: fp16 score operands, 0: bf16
+  unsigned long long limit_ns;  // time limit of every wait in the kernel
+  int inject_stall;      // failure-detection test only: withhold one barrier arrival
 };
 cudaError_t launch_attn_ws(const AttnTcParams& p, cudaStream_t stream);
 

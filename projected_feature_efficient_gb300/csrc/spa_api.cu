@@ -175,8 +175,11 @@ int run_prepare(const void* q, const void* k, const void* P, int B, int H, int N
 }
 
 // Stage 2: scores, mask, online softmax and the value product from a prepared workspace.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
 int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int causal,
-              int dtype, const void* ws, cudaStream_t stream) {
+              int dtype, const void* ws, cudaStream_t stream,
+              unsigned long long limit_ns = kWaitLimitNs, int inject_stall = 0) {
   const Layout L = make_layout(B, H, N, m, dtype);
   const int BH = B * H;
   const char* w = static_cast<const char*>(ws);
@@ -214,6 +217,8 @@ int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int
   ap.dv = dv;
   ap.causal = causal != 0;
   ap.f16_ops = L.mode == ProjOut::F16X1;
+  ap.limit_ns = limit_ns;
+  ap.inject_stall = inject_stall;
   return cuda_status(spa::launch_attn_ws(ap, stream));
 }
 
@@ -451,6 +456,37 @@ int spa_attention_fwd_host(const void* q, const void* k, const void* v, const vo
   return host_forward(static_cast<const char*>(q), static_cast<const char*>(k),
                       static_cast<const char*>(v), static_cast<const char*>(P), out, B, H, N, d, m,
                       d_v, causal, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int spa_selftest_wait_timeout(int limit_ms) {
+  if (limit_ms <= 0 || limit_ms > 2000) return SPA_ERR_SHAPE;
+  constexpr int B = 1, H = 1, N = 256, d = 64, m = 32, dv = 64;
+  const size_t nq = static_cast<size_t>(N) * d * 2, nv = static_cast<size_t>(N) * dv * 2;
+  const size_t np = static_cast<size_t>(d) * m * 2, no = static_cast<size_t>(N) * dv * 4;
+  const size_t oq = 0, ok = align256(oq + nq), ov = align256(ok + nq), op = align256(ov + nv),
+               oo = align256(op + np), ow = align256(oo + no);
+  const size_t total = ow + make_layout(B, H, N, m, SPA_BF16).total;
+  int* err = nullptr;
+  int st = device_error_ptr(&err);
+  if (st) return st;
+  char* buf = nullptr;
+  if (cudaMalloc(reinterpret_cast<void**>(&buf), total) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = cuda_status(cudaMemset(buf, 0, total));  // zero inputs: every score is 0
+  if (!st) st = run_prepare(buf + oq, buf + ok, buf + op, B, H, N, d, m, SPA_BF16, buf + ow, nullptr);
+  if (!st)
+    st = run_apply(buf + ov, reinterpret_cast<float*>(buf + oo), B, H, N, m, dv, 0, SPA_BF16,
+                   buf + ow, nullptr, static_cast<unsigned long long>(limit_ms) * 1000000ull, 1);
+  if (!st) st = cuda_status(cudaDeviceSynchronize());
+  int word = 0;
+  if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  if (!st) st = cuda_status(cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  cudaFree(buf);
+  if (st) return st;
+  return word ? SPA_ERR_TIMEOUT : SPA_OK;
 }
 
 int spa_device_error(int* code) {
