@@ -169,6 +169,39 @@ int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const
                               int dtype, void *stream);
 
 /*
+ * Decode with a projected key cache.  A decode step attends one new query per
+ * (batch, head) to all cached keys; with the projection it needs the cached
+ * K~ = K P_h (m values per key) instead of K (d values per key) ("Sparse
+ * Projection Attention", Sec. 3.1.2; the cache saving is the pages' argument
+ * for projected keys).  bf16 inputs only; d <= 256, m in {16,32,64,128}.
+ *
+ * Cache layout (caller-owned device memory, 16-byte aligned):
+ *   kc      [B][H][cap][m] fp16 (raw 16-bit values): K~ row j scaled by 2^-e_j
+ *   kc_mul  [B][H][cap]    fp32: 2^e_j, e_j chosen so that the row's max |value|
+ *                          lands in [2^13, 2^14) (every row at full fp16 precision)
+ *   v       [B][H][cap][d_v] bf16: the value cache, rows in the same order
+ *
+ * spa_kcache_append -- projects T new keys k [B][H][T][d] (bf16) with P
+ *   [H][d][m] and writes cache rows pos .. pos+T-1 of every (b, h) (fp32
+ *   products and sums, then the row exponent and fp16 rounding).  Rows are
+ *   independent: appending in pieces gives the same bits as one append.
+ *   SPA_ERR_SHAPE if pos + T > cap.  Asynchronous on `stream`.
+ *
+ * spa_attention_decode -- out[b][h][:] (fp32 [B][H][d_v]) =
+ *   softmax(q~ K~^T / sqrt(m)) V over cache rows 0 .. L-1 (1 <= L <= cap), with
+ *   q [B][H][d] bf16 and q~ = q P_h in fp32.  Scores, probabilities and P V are
+ *   fp32.  The keys are split into chunks processed in parallel and merged by a
+ *   log-sum-exp combine; the chunk results (B*H*chunks*(2+d_v) floats) are
+ *   taken with cudaMallocAsync on `stream` and released.  Equivalent to the
+ *   last row of the causal forward over the same L keys.
+ */
+int spa_kcache_append(const void *k, const void *P, void *kc, float *kc_mul, int B, int H, int T,
+                      int d, int m, int pos, int cap, int dtype, void *stream);
+int spa_attention_decode(const void *q, const void *P, const void *kc, const float *kc_mul,
+                         const void *v, float *out, int B, int H, int L, int d, int m, int d_v,
+                         int cap, int dtype, void *stream);
+
+/*
  * spa_selftest_wait_timeout -- failure-detection self-test (the pages have no
  * counterpart).  Runs one small bf16 forward (B=1 H=1 N=256 d=64 m=32 d_v=64,
  * zero inputs, buffers taken and released with cudaMalloc/cudaFree on the

@@ -46,6 +46,10 @@ lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
 lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
+lib.spa_kcache_append.argtypes = [_vp] * 4 + [_i] * 8 + [_vp]
+lib.spa_kcache_append.restype = _i
+lib.spa_attention_decode.argtypes = [_vp] * 6 + [_i] * 8 + [_vp]
+lib.spa_attention_decode.restype = _i
 
 
 class SpaError(RuntimeError):
@@ -179,6 +183,38 @@ def spa_attention_fwd_host(q, k, v, P, causal=False, out=None, stream=None):
     _check(lib.spa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), B, H, N, d,
                                       m, dv, int(bool(causal)), _dtype_code(q),
                                       _stream_ptr(stream)), "spa_attention_fwd_host")
+    return out
+
+
+def kcache_new(B, H, cap, m, device="cuda"):
+    """Empty projected key cache: (kc [B,H,cap,m] int16 holding fp16 bits,
+    kc_mul [B,H,cap] float32)."""
+    import torch
+    return (torch.zeros((B, H, cap, m), dtype=torch.int16, device=device),
+            torch.zeros((B, H, cap), dtype=torch.float32, device=device))
+
+
+def spa_kcache_append(k, P, kc, kc_mul, pos, stream=None):
+    """Project k [B,H,T,d] (bf16) with P [H,d,m] into cache rows pos..pos+T-1."""
+    B, H, T, d = k.shape
+    m = P.shape[2]
+    cap = kc.shape[2]
+    _check(lib.spa_kcache_append(_ptr(k), _ptr(P), _ptr(kc), _ptr(kc_mul), B, H, T, d, m, pos,
+                                 cap, _dtype_code(k), _stream_ptr(stream)), "spa_kcache_append")
+
+
+def spa_attention_decode(q, P, kc, kc_mul, v, L, out=None, stream=None):
+    """One query per (b, h): q [B,H,d] bf16 against cache rows 0..L-1 with the
+    value cache v [B,H,cap,dv] bf16; returns out [B,H,dv] float32."""
+    import torch
+    B, H, d = q.shape
+    m = P.shape[2]
+    cap, dv = v.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    _check(lib.spa_attention_decode(_ptr(q), _ptr(P), _ptr(kc), _ptr(kc_mul), _ptr(v), _ptr(out),
+                                    B, H, L, d, m, dv, cap, _dtype_code(q), _stream_ptr(stream)),
+           "spa_attention_decode")
     return out
 
 

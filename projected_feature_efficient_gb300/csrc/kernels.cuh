@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 namespace spa {
 
@@ -13,6 +14,7 @@ enum class ProjOut : int {
   F32 = 0,       // plain fp32 rows [BH][N][m]
   F16X1 = 1,     // fp16 UMMA tiles, power-of-two row (Q) / tile (K) exponents
   BF16X3 = 2,    // bf16 hi/lo split UMMA tiles, depth 3m
+  F16ROWS = 3,   // fp16 rows [BH][out_rows][m] at row out_pos + n, power-of-two row multipliers
 };
 
 // Score-GEMM operand tiles: 128 rows x KD columns of 16-bit values in the
@@ -35,6 +37,7 @@ struct ProjParams {
   int use_tc;            // tile modes: tensor-core kernel if the shape allows it
   CUtensorMap xmap[2];   // x[0], x[1] as 3-D (d, N, BH), bf16, 128-byte swizzle, box (64,128,1)
   int* err;              // device error word
+  int out_rows, out_pos; // F16ROWS: rows per (batch, head) of the output, first row written
 };
 bool project_tc_eligible(const ProjParams& p);
 cudaError_t launch_project(const ProjParams& p, cudaStream_t stream);
@@ -64,5 +67,21 @@ struct AttnF32Params {
   float scale;           // 1/sqrt(m)
 };
 cudaError_t launch_attn_f32(const AttnF32Params& p, cudaStream_t stream);
+
+// Single-query attention against the projected key cache, split over key chunks.
+constexpr int kDecodeMaxChunk = 8192;  // keys per chunk (scores in shared memory)
+struct DecodeParams {
+  const __nv_bfloat16* q;  // [BH][d] one query per (batch, head)
+  const __nv_bfloat16* P;  // [H][d][m]
+  const uint16_t* kc;      // [BH][cap][m]
+  const float* kc_mul;     // [BH][cap]
+  const __nv_bfloat16* v;  // [BH][cap][dv]
+  float* out;              // [BH][dv]
+  float* part;             // [BH][nsplit][2 + dv] chunk results (workspace)
+  int BH, H, L, d, m, dv, cap, nsplit, chunk;
+  float qscale;            // log2(e)/sqrt(m)
+};
+void decode_split(int BH, int L, int sms, int* nsplit, int* chunk);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace spa

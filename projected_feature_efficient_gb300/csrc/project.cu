@@ -24,6 +24,9 @@
 //           The attention kernel multiplies the raw scores back by both, which
 //           is exact.  Q also carries the factor log2(e)/sqrt(m) so the scores
 //           come out in base-2 logit units.
+//   F16ROWS projected key cache rows (decode): fp16, row-major [BH][rows][m],
+//           written at rows pos .. pos+N-1, each row divided by a power of two
+//           chosen from its own max |value| (multiplier kept per row).
 //   BF16X3  score-GEMM operand tiles in bf16, each value split v = hi + lo
 //           (hi = bf16(v), lo = bf16(v - hi)); Q rows are stored [hi|hi|lo] and
 //           K rows [hi|lo|hi], so one GEMM of depth 3m sums
@@ -66,6 +69,29 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, float (&acc)[MP]
                                            int bh, int which, int tid, float* red) {
   constexpr int KD = MODE == ProjOut::BF16X3 ? 3 * MP : MP;
   const int row = tile * kTileRows + tid;
+  if constexpr (MODE == ProjOut::F16ROWS) {
+    // projected key cache rows: fp16, row-major, one power-of-two multiplier per row
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < MP; ++k) amax = fmaxf(amax, fabsf(acc[k]));
+    const int e = range_exponent(amax);
+    const float down = pow2i(-e);
+    if (row < p.N) {
+      const size_t orow = static_cast<size_t>(bh) * p.out_rows + p.out_pos + row;
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out[0]) + orow * MP);
+#pragma unroll
+      for (int c8 = 0; c8 < MP / 8; ++c8) {
+        uint4 w;
+        w.x = f16_bits(acc[c8 * 8 + 0] * down) | (static_cast<uint32_t>(f16_bits(acc[c8 * 8 + 1] * down)) << 16);
+        w.y = f16_bits(acc[c8 * 8 + 2] * down) | (static_cast<uint32_t>(f16_bits(acc[c8 * 8 + 3] * down)) << 16);
+        w.z = f16_bits(acc[c8 * 8 + 4] * down) | (static_cast<uint32_t>(f16_bits(acc[c8 * 8 + 5] * down)) << 16);
+        w.w = f16_bits(acc[c8 * 8 + 6] * down) | (static_cast<uint32_t>(f16_bits(acc[c8 * 8 + 7] * down)) << 16);
+        o[c8] = w;
+      }
+      p.mul[0][orow] = pow2i(e);
+    }
+    return;
+  }
   uint16_t* tout = static_cast<uint16_t*>(which == 0 ? p.out[0] : p.out[1]) +
                    (static_cast<size_t>(bh) * p.NT + tile) * (kTileRows * KD);
   const float sc = which == 0 ? p.qscale : 1.f;
@@ -417,6 +443,23 @@ cudaError_t launch_project(const ProjParams& p, cudaStream_t stream) {
     return p.bf16_in ? launch_f32_out<__nv_bfloat16>(p, stream) : launch_f32_out<float>(p, stream);
   if (!p.bf16_in) return cudaErrorInvalidValue;
   const bool tc = p.use_tc && project_tc_eligible(p);
+  if (p.mode == ProjOut::F16ROWS) {
+    switch (p.m) {
+      case 16:
+        return tc ? launch_tc_mp<16, ProjOut::F16ROWS>(p, stream)
+                  : launch_one<__nv_bfloat16, 16, ProjOut::F16ROWS>(p, stream);
+      case 32:
+        return tc ? launch_tc_mp<32, ProjOut::F16ROWS>(p, stream)
+                  : launch_one<__nv_bfloat16, 32, ProjOut::F16ROWS>(p, stream);
+      case 64:
+        return tc ? launch_tc_mp<64, ProjOut::F16ROWS>(p, stream)
+                  : launch_one<__nv_bfloat16, 64, ProjOut::F16ROWS>(p, stream);
+      case 128:
+        return tc ? launch_tc_mp<128, ProjOut::F16ROWS>(p, stream)
+                  : launch_one<__nv_bfloat16, 128, ProjOut::F16ROWS>(p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (p.mode == ProjOut::BF16X3) {
     if (p.m != 16) return cudaErrorInvalidValue;
     return tc ? launch_tc_mp<16, ProjOut::BF16X3>(p, stream)

@@ -8,6 +8,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "../../include/spa.h"
@@ -456,6 +457,92 @@ int spa_attention_fwd_host(const void* q, const void* k, const void* v, const vo
   return host_forward(static_cast<const char*>(q), static_cast<const char*>(k),
                       static_cast<const char*>(v), static_cast<const char*>(P), out, B, H, N, d, m,
                       d_v, causal, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int spa_kcache_append(const void* k, const void* P, void* kc, float* kc_mul, int B, int H, int T,
+                      int d, int m, int pos, int cap, int dtype, void* stream) {
+  if (B < 0 || H < 0 || T < 0 || d < 0 || m < 0 || pos < 0 || cap < 0) return SPA_ERR_SHAPE;
+  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
+  if (static_cast<long long>(pos) + T > cap) return SPA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * T == 0) return SPA_OK;
+  if (static_cast<long long>(B) * H > 65535) return SPA_ERR_SHAPE;
+  if (dtype != SPA_BF16) return SPA_ERR_UNSUPPORTED;
+  if (d < 1 || d > 256 || (m != 16 && m != 32 && m != 64 && m != 128)) return SPA_ERR_UNSUPPORTED;
+  if (!k || !P || !kc || !kc_mul) return SPA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(P) || !aligned16(kc) || !aligned16(kc_mul)) return SPA_ERR_ALIGN;
+  // the projection kernels with a row-major fp16 output: rows pos .. pos+T-1
+  spa::ProjParams pp{};
+  pp.x[0] = k;
+  pp.P = P;
+  pp.out[0] = kc;
+  pp.mul[0] = kc_mul;
+  pp.nx = 1;
+  pp.BH = B * H;
+  pp.H = H;
+  pp.N = T;
+  pp.d = d;
+  pp.m = m;
+  pp.NT = (T + spa::kTileRows - 1) / spa::kTileRows;
+  pp.qscale = 1.f;
+  pp.bf16_in = 1;
+  pp.mode = ProjOut::F16ROWS;
+  pp.out_rows = cap;
+  pp.out_pos = pos;
+  pp.use_tc = 1;
+  if (spa::project_tc_eligible(pp)) {
+    int st;
+    if ((st = encode_bf16_rows(&pp.xmap[0], k, d, T, B * H))) return st;
+    if ((st = device_error_ptr(&pp.err))) return st;
+  }
+  return cuda_status(spa::launch_project(pp, static_cast<cudaStream_t>(stream)));
+}
+
+int spa_attention_decode(const void* q, const void* P, const void* kc, const float* kc_mul,
+                         const void* v, float* out, int B, int H, int L, int d, int m, int d_v,
+                         int cap, int dtype, void* stream) {
+  if (B < 0 || H < 0 || L < 0 || d < 0 || m < 0 || d_v < 0 || cap < 0) return SPA_ERR_SHAPE;
+  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
+  if (static_cast<long long>(B) * H == 0) return SPA_OK;
+  if (L < 1 || L > cap) return SPA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 65535) return SPA_ERR_SHAPE;
+  if (dtype != SPA_BF16) return SPA_ERR_UNSUPPORTED;
+  if (d < 1 || d > 256 || (m != 16 && m != 32 && m != 64 && m != 128) ||
+      (d_v != 64 && d_v != 128))
+    return SPA_ERR_UNSUPPORTED;
+  if (!q || !P || !kc || !kc_mul || !v || !out) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(P) || !aligned16(kc) || !aligned16(kc_mul) || !aligned16(v) ||
+      !aligned16(out))
+    return SPA_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPA_ERR_CUDA;
+  spa::DecodeParams dp{};
+  dp.q = static_cast<const __nv_bfloat16*>(q);
+  dp.P = static_cast<const __nv_bfloat16*>(P);
+  dp.kc = static_cast<const uint16_t*>(kc);
+  dp.kc_mul = kc_mul;
+  dp.v = static_cast<const __nv_bfloat16*>(v);
+  dp.out = out;
+  dp.BH = B * H;
+  dp.H = H;
+  dp.L = L;
+  dp.d = d;
+  dp.m = m;
+  dp.dv = d_v;
+  dp.cap = cap;
+  dp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m)));
+  spa::decode_split(dp.BH, L, sms, &dp.nsplit, &dp.chunk);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t part = static_cast<size_t>(dp.BH) * dp.nsplit * (2 + d_v) * sizeof(float);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&dp.part), part, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  const int st = cuda_status(spa::launch_decode(dp, s));
+  const cudaError_t fe = cudaFreeAsync(dp.part, s);
+  if (st) return st;
+  return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
 }
 
 int spa_selftest_wait_timeout(int limit_ms) {

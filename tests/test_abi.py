@@ -136,3 +136,38 @@ def test_binding_marshals_shapes():
         pkg.spa_attention_fwd(q, q, q, torch.zeros((3, 16, 16), dtype=torch.bfloat16))
     with pytest.raises(TypeError):
         pkg.spa_attention_fwd(q, q, q.float(), torch.zeros((2, 16, 16), dtype=torch.bfloat16))
+
+
+def append(lib, k=A, P=A, kc=A, kmul=A, B=1, H=2, T=4, d=128, m=32, pos=0, cap=16, dtype=BF16):
+    return lib.spa_kcache_append(k, P, kc, kmul, B, H, T, d, m, pos, cap, dtype, None)
+
+
+def decode(lib, q=A, P=A, kc=A, kmul=A, v=A, out=A, B=1, H=2, L=8, d=128, m=32, dv=128, cap=16,
+           dtype=BF16):
+    return lib.spa_attention_decode(q, P, kc, kmul, v, out, B, H, L, d, m, dv, cap, dtype, None)
+
+
+def test_cache_append_rejects_bad_arguments(lib):
+    assert append(lib, k=None) == NULL
+    assert append(lib, kmul=None) == NULL
+    assert append(lib, pos=13, T=4, cap=16) == SHAPE   # rows past the capacity
+    assert append(lib, pos=-1) == SHAPE
+    assert append(lib, dtype=F32) == UNSUPPORTED       # the fp16 cache is for bf16 inputs
+    assert append(lib, dtype=9) == DTYPE
+    assert append(lib, m=24) == UNSUPPORTED
+    assert append(lib, d=300) == UNSUPPORTED
+    assert append(lib, kc=A + 2) == ALIGN
+    assert append(lib, k=None, P=None, kc=None, kmul=None, T=0) == OK  # nothing to append
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert decode(lib, q=None) == NULL
+    assert decode(lib, v=None) == NULL
+    assert decode(lib, L=0) == SHAPE                    # no key to attend to
+    assert decode(lib, L=17, cap=16) == SHAPE           # more keys than the cache holds
+    assert decode(lib, dtype=F32) == UNSUPPORTED
+    assert decode(lib, dv=96) == UNSUPPORTED
+    assert decode(lib, m=48) == UNSUPPORTED
+    assert decode(lib, out=A + 4) == ALIGN
+    assert decode(lib, B=300, H=300) == SHAPE
+    assert decode(lib, q=None, P=None, kc=None, kmul=None, v=None, out=None, B=0) == OK
