@@ -10,6 +10,7 @@ with inputs resident in HBM.  The metric is TFLOP/s with
 and its fraction of the measured bf16 tensor-core peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --decode     (the decode row: projected key cache, workload D1)
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent problems, no data-path collective: weak scaling); rank 0 prints
@@ -413,6 +414,165 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+DECODE_METRIC = "projected-key-cache decode GB/s and % of measured GB300 HBM bandwidth"
+
+
+def decode_bytes(B, H, L, m, dv) -> int:
+    """Bytes a decode step must read: per key 2m (fp16 K~) + 4 (row multiplier)
+    + 2 d_v (bf16 V); the query and output rows are negligible."""
+    return B * H * L * (2 * m + 4 + 2 * dv)
+
+
+def run_decode(args, rank, world, local_rank):
+    """The decode row: one query per (batch, head) against the projected key
+    cache of workload D1 (cache filled once, outside the timed region)."""
+    import torch
+    import torch.distributed as dist
+
+    import projected_feature_efficient_gb300 as spa
+    import spa_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = si.WORKLOADS["D1"]
+    if args.decode_batch:
+        w = w.scaled(B=args.decode_batch)
+    B, H, L, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + w.number + 7919 * rank)
+    k = torch.randn((B, H, L, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, H, L, dv), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((B, H, d), generator=g, device=dev).to(torch.bfloat16)
+    P = (torch.randn((H, d, m), generator=g, device=dev) / math.sqrt(m)).to(torch.bfloat16)
+    kc, kmul = spa.kcache_new(B, H, L, m, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # prefill: project every key into the cache (timed separately, after a warm-up call)
+    spa.spa_kcache_append(k, P, kc, kmul, 0)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    spa.spa_kcache_append(k, P, kc, kmul, 0)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    append_ms = e0.elapsed_time(e1)
+    # CPU oracle baseline on heads of batch entry 0 (rank 0, one GPU only)
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        k0, v0, q0, P0 = k[0:1].cpu(), v[0:1].cpu(), q[0:1].cpu(), P.cpu()
+        done, t_used = 0, 0.0
+        while done < H and t_used < args.cpu_seconds / 2:
+            h = done
+            qf = torch.zeros((1, 1, L, d), dtype=torch.bfloat16)
+            qf[0, 0, L - 1] = q0[0, h]
+            t0 = time.perf_counter()
+            oracle.attention(qf, k0[:, h:h + 1], v0[:, h:h + 1], P0[h:h + 1], causal=True,
+                             rows=[L - 1])
+            t_used += time.perf_counter() - t0
+            done += 1
+        cpu = {"value": done * L * (2 * m + 4 + 2 * dv) / t_used / 1e9, "unit": "GB/s",
+               "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{done} of {B * H} (batch, head) decode rows, all {L} keys each, "
+                         f"including the fp64 projection of those keys; {t_used:.1f} s"}
+    del k
+    out = torch.empty((B, H, dv), dtype=torch.float32, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        spa.spa_attention_decode(q, P, kc, kmul, v, L, out=out)
+    barrier()
+    K = args.steps
+    sampler = ClockSampler(physical_device(local_rank))
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    barrier()
+    sampler.mark_start()
+    ev[0].record(stream)
+    for _ in range(K):
+        spa.spa_attention_decode(q, P, kc, kmul, v, L, out=out)
+    ev[1].record(stream)
+    barrier()
+    sampler.mark_end()
+    clocks = sampler.summary()
+    sampler.stop()
+    t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
+    nbytes = decode_bytes(B, H, L, m, dv)
+    value = world * nbytes * K / (t_ms * 1e-3) / 1e9
+
+    # end to end: the query from pinned host memory in, the output row out
+    q_h = q.cpu().pin_memory()
+    out_h = torch.empty((B, H, dv), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(q)
+    Ke = max(1, min(K, 20))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        q_d.copy_(q_h, non_blocking=True)
+        spa.spa_attention_decode(q_d, P, kc, kmul, v, L, out=out)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    te = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    if spa.device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
+
+    if rank == 0:
+        hbm = load_hbm_peak()
+        achieved = nbytes / (t_ms / K * 1e-3) / 1e9
+        line = {
+            "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": t_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"D1{'' if B == 8 else '-subset'}: decode, B={B} H={H} cached keys L={L} d={d} m={m} "
+                                   f"d_v={dv} bf16; K,V,q iid N(0,1); P iid N(0,1/m)",
+                       "B": B, "H": H, "L": L, "d": d, "m": m, "d_v": dv,
+                       "bytes_per_key": 2 * m + 4 + 2 * dv,
+                       "bytes_per_key_k_v_cache": 2 * d + 2 * dv,
+                       "l2": f"cache and values ({nbytes / 1e9:.2f} GB) larger than L2; no flush",
+                       "api": "spa_attention_decode on a resident cache",
+                       "parallelism": f"dp{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm[0], "unit": "GB/s",
+                         "frac": achieved / hbm[0], "traffic": None,
+                         "kernel": "decode_kernel + decode_combine_kernel (one step)",
+                         "peak_source": hbm[1]},
+            "e2e": {"value": world * nbytes * Ke / te / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": q_h.numel() * q_h.element_size(),
+                    "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+                    "api": "query copy in + spa_attention_decode + output copy out, synchronised",
+                    "steps": Ke},
+            "cache_append": {"ms": append_ms, "GB/s": B * H * L * (2 * d + 2 * m + 4) / append_ms / 1e6,
+                             "api": "spa_kcache_append of all L keys (prefill)"},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def load_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in pk and isinstance(pk[key], (int, float)):
+                return float(pk[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return 6800.0, "fallback"
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,12 +586,18 @@ def main(argv=None):
                     help="run C4 with fewer heads (smaller case for profiler captures)")
     ap.add_argument("--m", type=int, default=32, choices=(16, 32, 64),
                     help="projection width of the C4 sweep")
+    ap.add_argument("--decode", action="store_true",
+                    help="measure the decode row (projected key cache, workload D1) instead")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="decode with another batch size (smaller case for profiler captures)")
     args = ap.parse_args(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.decode:
+        return run_decode(args, rank, world, local_rank)
     return run_ours(args, rank, world, local_rank)
 
 

@@ -191,8 +191,8 @@ int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const
  *   softmax(q~ K~^T / sqrt(m)) V over cache rows 0 .. L-1 (1 <= L <= cap), with
  *   q [B][H][d] bf16 and q~ = q P_h in fp32.  Scores, probabilities and P V are
  *   fp32.  The keys are split into chunks processed in parallel and merged by a
- *   log-sum-exp combine; the chunk results (B*H*chunks*(2+d_v) floats) are
- *   taken with cudaMallocAsync on `stream` and released.  Equivalent to the
+ *   log-sum-exp combine; the chunk results (B*H*chunks*(2+d_v) floats) and
+ *   q~ (B*H*m floats) are taken with cudaMallocAsync on `stream` and released.  Equivalent to the
  *   last row of the causal forward over the same L keys.
  */
 int spa_kcache_append(const void *k, const void *P, void *kc, float *kc_mul, int B, int H, int T,

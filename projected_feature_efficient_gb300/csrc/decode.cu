@@ -11,8 +11,9 @@
 // The cache rows themselves are written by the projection kernels (project.cu,
 // output mode F16ROWS).
 //
+//   decode_qproj_kernel   q~ = q P_h (fp32) once per (batch, head).
 //   decode_kernel         one query per (batch, head) against keys 0 .. L-1,
-//                         split over key chunks: q~ = q P_h in fp32, scores
+//                         split over key chunks: scores
 //                         from the fp16 cache in fp32, chunk max and sum, and
 //                         the chunk's P V in fp32; writes (max, sum, O) per
 //                         chunk.  HBM-bound: per key 2m + 4 bytes of cache and
@@ -31,6 +32,17 @@ namespace {
 // ------------------------------------------------------------ decode
 constexpr int kDecodeThreads = 256;
 
+// q~ = q P_h * log2(e)/sqrt(m), once per (batch, head): grid BH, m threads.
+__global__ void __launch_bounds__(128) decode_qproj_kernel(const DecodeParams p) {
+  const int bh = blockIdx.x, h = bh % p.H, k = threadIdx.x;
+  if (k >= p.m) return;
+  const __nv_bfloat16* q = p.q + static_cast<size_t>(bh) * p.d;
+  const __nv_bfloat16* P = p.P + static_cast<size_t>(h) * p.d * p.m + k;
+  float acc = 0.f;
+  for (int l = 0; l < p.d; ++l) acc = fmaf(__bfloat162float(q[l]), __bfloat162float(P[l * p.m]), acc);
+  p.qproj[static_cast<size_t>(bh) * p.m + k] = acc * p.qscale;
+}
+
 // grid (nsplit, BH), 256 threads.  Chunk c covers keys [c*chunk, min(L, (c+1)*chunk)).
 template <int DV>
 __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeParams p) {
@@ -38,18 +50,12 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodePara
   __shared__ float qs[128];      // q~ * log2(e)/sqrt(m)
   __shared__ float red[kDecodeThreads / 32];
   __shared__ float oacc[kDecodeThreads / 32][DV];
-  const int bh = blockIdx.y, h = bh % p.H, split = blockIdx.x;
+  const int bh = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = split * p.chunk, n = min(p.L, k0 + p.chunk) - k0;
 
-  // q~ = q P_h in fp32 (d products per output)
-  const __nv_bfloat16* q = p.q + static_cast<size_t>(bh) * p.d;
-  const __nv_bfloat16* P = p.P + static_cast<size_t>(h) * p.d * p.m;
-  for (int k = tid; k < p.m; k += kDecodeThreads) {
-    float acc = 0.f;
-    for (int l = 0; l < p.d; ++l) acc = fmaf(__bfloat162float(q[l]), __bfloat162float(P[l * p.m + k]), acc);
-    qs[k] = acc * p.qscale;
-  }
+  // q~ (projected and scaled once per (batch, head) by decode_qproj_kernel)
+  for (int k = tid; k < p.m; k += kDecodeThreads) qs[k] = p.qproj[static_cast<size_t>(bh) * p.m + k];
   __syncthreads();
 
   // scores in log2 units: one key row per thread, m fp16 values in 16-byte pieces
@@ -174,7 +180,7 @@ void decode_split(int BH, int L, int sms, int* nsplit, int* chunk) {
   // and at most kDecodeMaxChunk (its scores stay in shared memory)
   const long long want = (8LL * sms + BH - 1) / BH;
   int ns = static_cast<int>(want < 1 ? 1 : want);
-  const int by_len = (L + 63) / 64;  // at least 64 keys per chunk
+  const int by_len = (L + 255) / 256;  // at least 256 keys per chunk
   if (ns > by_len) ns = by_len;
   const int min_ns = (L + kDecodeMaxChunk - 1) / kDecodeMaxChunk;
   if (ns < min_ns) ns = min_ns;
@@ -188,6 +194,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(p.chunk) * sizeof(float);
   dim3 grid(p.nsplit, p.BH);
   cudaError_t e;
+  decode_qproj_kernel<<<p.BH, 128, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.dv == 128) {
     e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));

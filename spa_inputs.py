@@ -74,6 +74,9 @@ WORKLOADS = {
 }
 # exact-attention control on the C5 inputs: m = d = 128 and P = I
 WORKLOADS["C5ctl"] = replace(WORKLOADS["C5"], name="C5ctl", m=128, identity_P=True)
+# decode with the projected key cache: one query per (batch, head) against N
+# cached keys (the last causal row), C4-sized heads at batch 8
+WORKLOADS["D1"] = Workload("D1", 6, 8, 32, 32768, 128, 32, 128, "bf16", True, "iid")
 
 
 def _normalise_rows(x: torch.Tensor, target: float) -> torch.Tensor:

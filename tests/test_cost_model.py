@@ -67,3 +67,13 @@ def test_workload_flops(B, H, N, d, m, dv, causal, gflops):
     # the convention halves N^2 instead of counting N(N+1)/2 pairs
     assert bench.flops(B, H, N, d, m, dv, causal) == pytest.approx(exact_causal,
                                                                    rel=2.0 / N if causal else 0)
+
+
+def test_decode_bytes_per_step():
+    """A decode step reads, per cached key, m fp16 values and one fp32 multiplier
+    of the projected key cache plus d_v bf16 values: 324 bytes at m=32, d_v=128,
+    against 512 for a cache of K and V at d=128."""
+    assert bench.decode_bytes(1, 1, 1, 32, 128) == 324
+    assert bench.decode_bytes(8, 32, 32768, 32, 128) == 8 * 32 * 32768 * 324
+    ratio = bench.decode_bytes(1, 1, 1, 32, 128) / (2 * 128 + 2 * 128)
+    assert abs(ratio - 0.6328125) < 1e-12
