@@ -55,6 +55,8 @@ def _bind(path):
     lib.orc_attention.restype = i
     lib.orc_num_threads.argtypes = []
     lib.orc_num_threads.restype = i
+    lib.orc_attention_bwd.argtypes = [vp, vp, vp, vp, vp, i, dp, dp, dp, dp, i, i, l, i, i, i, i]
+    lib.orc_attention_bwd.restype = i
     return lib
 
 
@@ -159,3 +161,30 @@ def compile_variant(src_text: str, out_dir: str):
 def source() -> str:
     with open(_SRC) as f:
         return f.read()
+
+
+def attention_bwd(q, k, v, P, dO, causal: bool = False, _lib=None):
+    """fp64 gradients of O = softmax((qP)(kP)^T / sqrt(m)) v for the upstream
+    gradient dO [B,H,N,dv] (same element type as the inputs).
+
+    Returns (dq [B,H,N,d], dk [B,H,N,d], dv [B,H,N,dv], dP [H,d,m]) as float64.
+    """
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    m = P.shape[-1]
+    assert tuple(k.shape) == (B, H, N, d) and tuple(v.shape) == (B, H, N, dv)
+    assert tuple(P.shape) == (H, d, m) and tuple(dO.shape) == (B, H, N, dv)
+    raws = [_as_raw(t) for t in (q, k, v, P, dO)]
+    codes = {r[2] for r in raws}
+    assert len(codes) == 1, "q, k, v, P, dO must share one element type"
+    code = codes.pop()
+    dq = np.empty((B, H, N, d), dtype=np.float64)
+    dk = np.empty((B, H, N, d), dtype=np.float64)
+    dvo = np.empty((B, H, N, dv), dtype=np.float64)
+    dP = np.empty((H, d, m), dtype=np.float64)
+    rc = (_lib or _load()).orc_attention_bwd(
+        raws[0][1], raws[1][1], raws[2][1], raws[3][1], raws[4][1], code, dq.ctypes.data,
+        dk.ctypes.data, dvo.ctypes.data, dP.ctypes.data, B, H, N, d, m, dv, int(bool(causal)))
+    if rc:
+        raise ValueError(f"orc_attention_bwd failed ({rc})")
+    return dq, dk, dvo, dP

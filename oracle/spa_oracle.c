@@ -27,9 +27,11 @@
  * Element types accepted for inputs: 0 = double, 1 = float, 2 = bfloat16
  * (raw 16-bit patterns).  Widening bf16 -> double is exact.
  *
- * Parity status: both entry points are pinned by the tests in
+ * Parity status: every entry point is pinned by the tests in
  * tests/test_oracle_pins.py (a library attention routine, closed forms,
- * brute-force cases, softmax/JL invariants stated on the pages).
+ * brute-force cases, softmax/JL invariants stated on the pages; for the
+ * gradients, central finite differences, automatic differentiation of a
+ * plain restatement of the forward, and exact sum rules).
  */
 #include <math.h>
 #include <stdint.h>
@@ -162,5 +164,157 @@ int orc_attention(const void *q, const void *k, const void *v, const void *P, in
         }
     }
     free(kp);
+    return 0;
+}
+
+/*
+ * Gradients of the forward above, for a given upstream gradient dO of the
+ * output (same element type as the inputs), by the chain rule through each
+ * step, per (batch b, head h):
+ *   A_ij   = exp(s_ij - M_i) / l_i                 (the forward's softmax)
+ *   O_i    = sum_j A_ij V_j
+ *   dV_j   = sum_i A_ij dO_i                       (step 6, w.r.t. V)
+ *   dA_ij  = <dO_i, V_j>                           (step 6, w.r.t. A)
+ *   D_i    = sum_j A_ij dA_ij = <dO_i, O_i>
+ *   dS_ij  = A_ij (dA_ij - D_i)                    (step 5: softmax Jacobian)
+ *   dQp_i  = sum_j dS_ij Kp_j / sqrt(m)            (step 3)
+ *   dKp_j  = sum_i dS_ij Qp_i / sqrt(m)
+ *   dQ_i   = dQp_i P_h^T,  dK_j = dKp_j P_h^T      (step 2)
+ *   dP_h  += sum_i Q_i^T dQp_i + sum_j K_j^T dKp_j  (step 2, w.r.t. P; P_h is
+ *                                                    shared by every batch entry)
+ * with the causal mask (j <= i) applied to every sum over j or i.
+ * ("Sparse Projection Attention", Sec. 3.4.1 and Algorithm 2: the projection
+ *  is trained through these gradients.)
+ * Outputs (double): dq, dk [B][H][N][d]; dv_out [B][H][N][dv]; dP [H][d][m].
+ */
+int orc_attention_bwd(const void *q, const void *k, const void *v, const void *P,
+                      const void *dO, int dt, double *dq, double *dk, double *dv_out,
+                      double *dP, int B, int H, long N, int d, int m, int dv, int causal)
+{
+    if (!q || !k || !v || !P || !dO || !dq || !dk || !dv_out || !dP || B < 0 || H < 0 ||
+        N < 0 || d <= 0 || m <= 0 || dv <= 0)
+        return 1;
+    memset(dP, 0, sizeof(double) * (size_t)H * d * m);
+    if (N == 0) return 0;
+    const double rsm = 1.0 / sqrt((double)m); /* 1/sqrt(m) */
+    double *qp = (double *)malloc(sizeof(double) * (size_t)N * m);
+    double *kp = (double *)malloc(sizeof(double) * (size_t)N * m);
+    double *dqp = (double *)malloc(sizeof(double) * (size_t)N * m);
+    double *dkp = (double *)malloc(sizeof(double) * (size_t)N * m);
+    double *rmax = (double *)malloc(sizeof(double) * (size_t)N);
+    double *rsum = (double *)malloc(sizeof(double) * (size_t)N);
+    double *rdot = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!qp || !kp || !dqp || !dkp || !rmax || !rsum || !rdot) {
+        free(qp); free(kp); free(dqp); free(dkp); free(rmax); free(rsum); free(rdot);
+        return 3;
+    }
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const size_t bh = (size_t)b * H + h;
+            const size_t p_off = (size_t)h * d * m;
+            #pragma omp parallel for schedule(static)
+            for (long i = 0; i < N; ++i) {
+                orc_project_row(q, dt, (bh * N + i) * d, P, p_off, d, m, qp + (size_t)i * m);
+                orc_project_row(k, dt, (bh * N + i) * d, P, p_off, d, m, kp + (size_t)i * m);
+            }
+            /* pass 1, per row: M_i, l_i and D_i = <dO_i, O_i> */
+            #pragma omp parallel
+            {
+                double *o = (double *)malloc(sizeof(double) * (size_t)dv);
+                #pragma omp for schedule(dynamic, 4)
+                for (long i = 0; i < N; ++i) {
+                    const long kcount = causal ? i + 1 : N; /* keys row i sees */
+                    double mx = -INFINITY;
+                    for (long j = 0; j < kcount; ++j) {
+                        double acc = 0.0;
+                        for (int c = 0; c < m; ++c) acc += qp[(size_t)i * m + c] * kp[(size_t)j * m + c];
+                        if (acc * rsm > mx) mx = acc * rsm;
+                    }
+                    double l = 0.0;
+                    for (int c = 0; c < dv; ++c) o[c] = 0.0;
+                    for (long j = 0; j < kcount; ++j) {
+                        double acc = 0.0;
+                        for (int c = 0; c < m; ++c) acc += qp[(size_t)i * m + c] * kp[(size_t)j * m + c];
+                        const double e = exp(acc * rsm - mx);
+                        l += e;
+                        for (int c = 0; c < dv; ++c) o[c] += e * orc_load(v, dt, (bh * N + j) * dv + c);
+                    }
+                    double dot = 0.0;
+                    for (int c = 0; c < dv; ++c) dot += orc_load(dO, dt, (bh * N + i) * dv + c) * (o[c] / l);
+                    rmax[i] = mx;
+                    rsum[i] = l;
+                    rdot[i] = dot;
+                }
+                free(o);
+            }
+            /* A_ij and dS_ij, recomputed where needed */
+            #define ORC_A(i, j, out_a, out_ds)                                                 \
+                do {                                                                           \
+                    double acc_ = 0.0;                                                         \
+                    for (int c_ = 0; c_ < m; ++c_)                                             \
+                        acc_ += qp[(size_t)(i) * m + c_] * kp[(size_t)(j) * m + c_];           \
+                    const double a_ = exp(acc_ * rsm - rmax[i]) / rsum[i];              \
+                    double da_ = 0.0;                                                          \
+                    for (int c_ = 0; c_ < dv; ++c_)                                            \
+                        da_ += orc_load(dO, dt, (bh * N + (i)) * dv + c_) *                    \
+                               orc_load(v, dt, (bh * N + (j)) * dv + c_);                      \
+                    (out_a) = a_;                                                              \
+                    (out_ds) = a_ * (da_ - rdot[i]);                                           \
+                } while (0)
+            /* pass 2a, per row: dQp_i */
+            #pragma omp parallel for schedule(dynamic, 4)
+            for (long i = 0; i < N; ++i) {
+                double *g = dqp + (size_t)i * m;
+                for (int c = 0; c < m; ++c) g[c] = 0.0;
+                const long kcount = causal ? i + 1 : N; /* keys row i sees */
+                for (long j = 0; j < kcount; ++j) {
+                    double a, ds;
+                    ORC_A(i, j, a, ds);
+                    (void)a;
+                    for (int c = 0; c < m; ++c) g[c] += ds * kp[(size_t)j * m + c] * rsm;
+                }
+            }
+            /* pass 2b, per key: dKp_j and dV_j */
+            #pragma omp parallel for schedule(dynamic, 4)
+            for (long j = 0; j < N; ++j) {
+                double *g = dkp + (size_t)j * m;
+                double *gv = dv_out + (bh * N + j) * dv;
+                for (int c = 0; c < m; ++c) g[c] = 0.0;
+                for (int c = 0; c < dv; ++c) gv[c] = 0.0;
+                for (long i = causal ? j : 0; i < N; ++i) {
+                    double a, ds;
+                    ORC_A(i, j, a, ds);
+                    for (int c = 0; c < m; ++c) g[c] += ds * qp[(size_t)i * m + c] * rsm;
+                    for (int c = 0; c < dv; ++c) gv[c] += a * orc_load(dO, dt, (bh * N + i) * dv + c);
+                }
+            }
+            #undef ORC_A
+            /* step 2 backwards: dQ = dQp P^T, dK = dKp P^T, dP_h += Q^T dQp + K^T dKp */
+            #pragma omp parallel for schedule(static)
+            for (long i = 0; i < N; ++i) {
+                for (int l = 0; l < d; ++l) {
+                    double aq = 0.0, ak = 0.0;
+                    for (int c = 0; c < m; ++c) {
+                        const double p = orc_load(P, dt, p_off + (size_t)l * m + c);
+                        aq += dqp[(size_t)i * m + c] * p;
+                        ak += dkp[(size_t)i * m + c] * p;
+                    }
+                    dq[(bh * N + i) * d + l] = aq;
+                    dk[(bh * N + i) * d + l] = ak;
+                }
+            }
+            #pragma omp parallel for schedule(static)
+            for (int l = 0; l < d; ++l) {
+                for (int c = 0; c < m; ++c) {
+                    double acc = 0.0;
+                    for (long i = 0; i < N; ++i)
+                        acc += orc_load(q, dt, (bh * N + i) * d + l) * dqp[(size_t)i * m + c] +
+                               orc_load(k, dt, (bh * N + i) * d + l) * dkp[(size_t)i * m + c];
+                    dP[p_off + (size_t)l * m + c] += acc;
+                }
+            }
+        }
+    }
+    free(qp); free(kp); free(dqp); free(dkp); free(rmax); free(rsum); free(rdot);
     return 0;
 }

@@ -1,7 +1,10 @@
 """The oracle's pins have teeth: copies of the oracle with one planted mistake
 (compiled on the CPU into a temporary directory) must fail them.  The planted
 mistakes are the plausible ones: a wrong score scale, an off-by-one causal
-mask, a transposed projection, a missing normalisation, a wrong value row."""
+mask, a transposed projection, a missing normalisation, a wrong value row; and
+in the gradients, a softmax Jacobian without its row term, a key gradient
+built from the wrong operand, a value gradient with the wrong weight, masked
+rows leaking into the key gradients, a projection gradient missing the keys."""
 import math
 
 import numpy as np
@@ -58,3 +61,36 @@ def test_planted_mistake_is_caught(name, tmp_path):
     assert src.count(old) == 1, f"mutation site for {name} not found"
     lib = oracle.compile_variant(src.replace(old, new), str(tmp_path))
     assert not pins_pass(lib), f"pins did not catch mutant {name}"
+
+
+# ---------------------------------------------------------------- gradients
+BWD_MUTANTS = {
+    "softmax_grad_without_row_dot": ("(out_ds) = a_ * (da_ - rdot[i]);", "(out_ds) = a_ * da_;"),
+    "key_grad_from_keys": ("g[c] += ds * qp[(size_t)i * m + c] * rsm;",
+                           "g[c] += ds * kp[(size_t)i * m + c] * rsm;"),
+    "value_grad_weighted_by_ds": ("gv[c] += a * orc_load(dO, dt, (bh * N + i) * dv + c);",
+                                  "gv[c] += ds * orc_load(dO, dt, (bh * N + i) * dv + c);"),
+    "masked_rows_in_key_grads": ("for (long i = causal ? j : 0; i < N; ++i) {",
+                                 "for (long i = 0; i < N; ++i) {"),
+    "projection_grad_misses_keys": ("orc_load(k, dt, (bh * N + i) * d + l) * dkp[(size_t)i * m + c];",
+                                    "0.0 * dkp[(size_t)i * m + c];"),
+}
+
+
+def bwd_pins_pass(lib) -> bool:
+    from test_oracle_bwd import finite_difference_pins
+    return all(finite_difference_pins(lib, causal=c) for c in (False, True))
+
+
+def test_unmodified_copy_passes_gradient_pins(tmp_path):
+    lib = oracle.compile_variant(oracle.source(), str(tmp_path))
+    assert bwd_pins_pass(lib)
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_planted_gradient_mistake_is_caught(name, tmp_path):
+    old, new = BWD_MUTANTS[name]
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation site for {name} not found"
+    lib = oracle.compile_variant(src.replace(old, new), str(tmp_path))
+    assert not bwd_pins_pass(lib), f"gradient pins did not catch mutant {name}"
