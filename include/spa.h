@@ -202,6 +202,30 @@ int spa_attention_decode(const void *q, const void *P, const void *kc, const flo
                          int cap, int dtype, void *stream);
 
 /*
+ * Sparse Feature Attention ("Scaling Attention via Feature Sparsity" notes,
+ * Sec. 1 and Sec. 3): every query and key row keeps its k features of largest
+ * magnitude and zeroes the rest, and attention runs on the sparsified rows,
+ * softmax(Topk(Q) Topk(K)^T / sqrt(d)) V.  The dense tensor-core forward does
+ * the attention (the pages' sparse-intersection kernel is a different design
+ * and is not built).
+ *
+ * spa_topk_features -- y[r] = Topk_k(x[r]) for rows r of x [rows][d] (bf16 or
+ *   fp32; y the same type; d in {32, 64, 128, 256}; 1 <= k <= d).  Ties at the
+ *   k-th magnitude keep the lowest feature indices.  The selection compares
+ *   the exact input values, so it is bit-exact; inputs must be finite.
+ *
+ * spa_sfa_attention_fwd -- out [B][H][N][d_v] fp32 = the forward above with
+ *   q, k sparsified to topk features per row, i.e. spa_attention_fwd of
+ *   (Topk(q), Topk(k), v) with P_h = I_d (m = d, scale 1/sqrt(d)).  d in
+ *   {32, 64, 128}.  The sparsified copies, the identity P and the workspace
+ *   are taken with cudaMallocAsync on `stream` and released.
+ */
+int spa_topk_features(const void *x, void *y, long long rows, int d, int k, int dtype,
+                      void *stream);
+int spa_sfa_attention_fwd(const void *q, const void *k, const void *v, float *out, int B, int H,
+                          int N, int d, int d_v, int topk, int causal, int dtype, void *stream);
+
+/*
  * spa_selftest_wait_timeout -- failure-detection self-test (the pages have no
  * counterpart).  Runs one small bf16 forward (B=1 H=1 N=256 d=64 m=32 d_v=64,
  * zero inputs, buffers taken and released with cudaMalloc/cudaFree on the

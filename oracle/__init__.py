@@ -188,3 +188,19 @@ def attention_bwd(q, k, v, P, dO, causal: bool = False, _lib=None):
     if rc:
         raise ValueError(f"orc_attention_bwd failed ({rc})")
     return dq, dk, dvo, dP
+
+
+def topk_features(x, k: int) -> np.ndarray:
+    """Row-wise Top-k over the last axis ("Scaling Attention via Feature
+    Sparsity" notes, Sec. 1): keep the k entries of largest magnitude, zero the
+    rest.  Ties at the k-th magnitude keep the lowest indices (a stable sort on
+    the negated exact magnitudes).  Returns float64 with exact copies of the
+    kept values (signed zeros included)."""
+    xs = np.asarray(x.double().numpy() if hasattr(x, "double") else x, dtype=np.float64)
+    d = xs.shape[-1]
+    flat = xs.reshape(-1, d)
+    out = np.zeros_like(flat)
+    for r in range(flat.shape[0]):
+        order = np.argsort(-np.abs(flat[r]), kind="stable")[:k]
+        out[r, order] = flat[r, order]
+    return out.reshape(xs.shape)

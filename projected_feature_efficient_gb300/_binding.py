@@ -46,6 +46,10 @@ lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
 lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
+lib.spa_topk_features.argtypes = [_vp, _vp, ctypes.c_longlong, _i, _i, _i, _vp]
+lib.spa_topk_features.restype = _i
+lib.spa_sfa_attention_fwd.argtypes = [_vp] * 4 + [_i] * 8 + [_vp]
+lib.spa_sfa_attention_fwd.restype = _i
 lib.spa_kcache_append.argtypes = [_vp] * 4 + [_i] * 8 + [_vp]
 lib.spa_kcache_append.restype = _i
 lib.spa_attention_decode.argtypes = [_vp] * 6 + [_i] * 8 + [_vp]
@@ -183,6 +187,31 @@ def spa_attention_fwd_host(q, k, v, P, causal=False, out=None, stream=None):
     _check(lib.spa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), B, H, N, d,
                                       m, dv, int(bool(causal)), _dtype_code(q),
                                       _stream_ptr(stream)), "spa_attention_fwd_host")
+    return out
+
+
+def spa_topk_features(x, k, out=None, stream=None):
+    """Row-wise Top-k over the last dimension of x (bf16 or fp32 CUDA tensor)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(x)
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    _check(lib.spa_topk_features(_ptr(x), _ptr(out), rows, d, int(k), _dtype_code(x),
+                                 _stream_ptr(stream)), "spa_topk_features")
+    return out
+
+
+def spa_sfa_attention_fwd(q, k, v, topk, causal=False, out=None, stream=None):
+    """softmax(Topk(q) Topk(k)^T / sqrt(d)) v; q, k [B,H,N,d], v [B,H,N,dv]."""
+    import torch
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    _check(lib.spa_sfa_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, N, d, dv,
+                                     int(topk), int(bool(causal)), _dtype_code(q),
+                                     _stream_ptr(stream)), "spa_sfa_attention_fwd")
     return out
 
 

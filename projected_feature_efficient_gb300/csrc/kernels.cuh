@@ -68,6 +68,18 @@ struct AttnF32Params {
 };
 cudaError_t launch_attn_f32(const AttnF32Params& p, cudaStream_t stream);
 
+// Row-wise Top-k feature sparsification: y[r] keeps the k largest-magnitude
+// features of x[r] (ties: lowest feature index first) and zeroes the rest.
+struct TopkParams {
+  const void* x;  // [rows][d], bf16 or fp32
+  void* y;        // [rows][d], same type
+  long long rows;
+  int d, k;       // d in {32, 64, 128, 256}, 1 <= k <= d
+  int bf16;       // element type: 1 = bf16, 0 = fp32
+};
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream);  // P[h] = I_d
+
 // Single-query attention against the projected key cache, split over key chunks.
 constexpr int kDecodeMaxChunk = 8192;  // keys per chunk (scores in shared memory)
 struct DecodeParams {

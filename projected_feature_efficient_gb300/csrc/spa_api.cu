@@ -547,6 +547,58 @@ int spa_attention_decode(const void* q, const void* P, const void* kc, const flo
   return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
 }
 
+int spa_topk_features(const void* x, void* y, long long rows, int d, int k, int dtype,
+                      void* stream) {
+  if (rows < 0 || d < 0 || k < 0) return SPA_ERR_SHAPE;
+  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
+  if (rows == 0) return SPA_OK;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return SPA_ERR_UNSUPPORTED;
+  if (k < 1 || k > d) return SPA_ERR_SHAPE;
+  if (!x || !y) return SPA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y)) return SPA_ERR_ALIGN;
+  spa::TopkParams tp{};
+  tp.x = x;
+  tp.y = y;
+  tp.rows = rows;
+  tp.d = d;
+  tp.k = k;
+  tp.bf16 = dtype == SPA_BF16;
+  return cuda_status(spa::launch_topk(tp, static_cast<cudaStream_t>(stream)));
+}
+
+int spa_sfa_attention_fwd(const void* q, const void* k, const void* v, float* out, int B, int H,
+                          int N, int d, int d_v, int topk, int causal, int dtype, void* stream) {
+  // the forward with P = I_d (m = d): scale 1/sqrt(d) on the sparsified rows
+  int st = check_shape(B, H, N, d, d, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if (d != 32 && d != 64 && d != 128) return SPA_ERR_UNSUPPORTED;
+  if (topk < 1 || topk > d) return SPA_ERR_SHAPE;
+  if (!q || !k || !v || !out) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SPA_ERR_ALIGN;
+  const size_t es = dtype == SPA_BF16 ? 2 : 4;
+  const long long rows = static_cast<long long>(B) * H * N;
+  const size_t nq = static_cast<size_t>(rows) * d * es;
+  const size_t np = static_cast<size_t>(H) * d * d * es;
+  const size_t oq = 0, ok = align256(oq + nq), op = align256(ok + nq), ow = align256(op + np);
+  const size_t total = ow + make_layout(B, H, N, d, dtype).total;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* buf = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&buf), total, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = spa_topk_features(q, buf + oq, rows, d, topk, dtype, stream);
+  if (!st) st = spa_topk_features(k, buf + ok, rows, d, topk, dtype, stream);
+  if (!st) st = cuda_status(spa::launch_identity(buf + op, H, d, dtype == SPA_BF16, s));
+  if (!st)
+    st = run_forward(buf + oq, buf + ok, v, buf + op, out, B, H, N, d, d, d_v, causal, dtype,
+                     buf + ow, s);
+  const cudaError_t fe = cudaFreeAsync(buf, s);
+  if (st) return st;
+  return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
+}
+
 int spa_selftest_wait_timeout(int limit_ms) {
   if (limit_ms <= 0 || limit_ms > 2000) return SPA_ERR_SHAPE;
   constexpr int B = 1, H = 1, N = 256, d = 64, m = 32, dv = 64;

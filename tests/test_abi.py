@@ -171,3 +171,17 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode(lib, out=A + 4) == ALIGN
     assert decode(lib, B=300, H=300) == SHAPE
     assert decode(lib, q=None, P=None, kc=None, kmul=None, v=None, out=None, B=0) == OK
+
+
+def test_topk_and_sfa_reject_bad_arguments(lib):
+    assert lib.spa_topk_features(A, A, 10, 96, 4, BF16, None) == UNSUPPORTED   # d not 32/64/128/256
+    assert lib.spa_topk_features(A, A, 10, 128, 0, BF16, None) == SHAPE       # k < 1
+    assert lib.spa_topk_features(A, A, 10, 128, 129, BF16, None) == SHAPE     # k > d
+    assert lib.spa_topk_features(None, A, 10, 128, 4, BF16, None) == NULL
+    assert lib.spa_topk_features(A, A + 2, 10, 128, 4, BF16, None) == ALIGN
+    assert lib.spa_topk_features(None, None, 0, 128, 4, BF16, None) == OK     # no rows
+    sfa = lib.spa_sfa_attention_fwd
+    assert sfa(A, A, A, A, 1, 2, 64, 256, 128, 8, 0, BF16, None) == UNSUPPORTED  # m = d = 256
+    assert sfa(A, A, A, A, 1, 2, 64, 128, 128, 0, 0, BF16, None) == SHAPE
+    assert sfa(A, None, A, A, 1, 2, 64, 128, 128, 8, 0, BF16, None) == NULL
+    assert sfa(None, None, None, None, 1, 2, 0, 128, 128, 8, 0, BF16, None) == OK

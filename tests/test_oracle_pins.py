@@ -308,3 +308,45 @@ def test_score_error_decays_like_inverse_sqrt_m():
         errs.append(e / 20)
     slope = np.polyfit(np.log(ms), np.log(errs), 1)[0]
     assert -0.65 <= slope <= -0.35, slope
+
+
+# ------------------------------------------------------------ Top-k features
+def test_topk_worked_example_with_ties():
+    """|x| = 1, 2, 2, 2, 0.5: the top two are the first two of the three tied 2s."""
+    x = np.array([[1.0, -2.0, 2.0, 2.0, 0.5]])
+    np.testing.assert_array_equal(oracle.topk_features(x, 2), [[0.0, -2.0, 2.0, 0.0, 0.0]])
+    np.testing.assert_array_equal(oracle.topk_features(x, 1), [[0.0, -2.0, 0.0, 0.0, 0.0]])
+    np.testing.assert_array_equal(oracle.topk_features(x, 5), x)
+
+
+def test_topk_brute_force_on_small_rows():
+    """Against brute force over every k-subset: the kept set has the largest
+    sum of magnitudes, and among equal sums the lexicographically smallest
+    index set (lowest indices first)."""
+    import itertools
+    rng = np.random.default_rng(4)
+    for _ in range(60):
+        d = int(rng.integers(1, 7))
+        k = int(rng.integers(1, d + 1))
+        x = rng.choice([-2.0, -1.0, -0.5, 0.5, 1.0, 2.0, 3.0], size=d)
+        best = None
+        for sub in itertools.combinations(range(d), k):
+            key = (-sum(abs(x[i]) for i in sub), sub)
+            if best is None or key < best:
+                best = key
+        want = np.zeros(d)
+        want[list(best[1])] = x[list(best[1])]
+        np.testing.assert_array_equal(oracle.topk_features(x[None], k)[0], want)
+
+
+def test_topk_invariants_on_random_rows():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((50, 128))
+    for k in (1, 16, 127, 128):
+        y = oracle.topk_features(x, k)
+        kept = y != 0
+        assert np.all(kept.sum(axis=1) == k)
+        assert np.all(y[kept] == x[kept])
+        for r in range(x.shape[0]):
+            if k < 128:
+                assert np.abs(x[r][~kept[r]]).max() <= np.abs(x[r][kept[r]]).min()
