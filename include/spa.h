@@ -169,6 +169,27 @@ int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const
                               int dtype, void *stream);
 
 /*
+ * spa_attention_bwd -- gradients of spa_attention_fwd for an upstream gradient
+ * dO [B][H][N][d_v] (same type as the inputs), given the forward's output out
+ * (fp32).  Writes dq, dk [B][H][N][d], dv [B][H][N][d_v] and dP [H][d][m] (the
+ * projection is shared by the batch: dP sums over it), all fp32:
+ *   A = softmax(Qp Kp^T / sqrt(m)) (causal: keys j <= i), D_i = <dO_i, out_i>,
+ *   dS = A * (dO V^T - D) / sqrt(m), dQp = dS Kp, dKp = dS^T Qp, dV = A^T dO,
+ *   dq = dQp P_h^T, dk = dKp P_h^T, dP_h = sum_b (q^T dQp + k^T dKp)
+ * ("Sparse Projection Attention", Sec. 3.4.1; Algorithm 2 trains P through
+ * these).  This version materialises A and dS for as many heads as fit in
+ * 8 GB at a time (2 N^2 floats per head) and uses cuBLAS for the plain
+ * products (fp32 accumulation; TF32 products for bf16 inputs, exact for
+ * their values; fp32 products for fp32 inputs).  d <= 128; the other limits
+ * are the forward's.  Workspace from cudaMallocAsync on `stream`.  An empty
+ * problem (B*H*N == 0) zeroes dP.
+ */
+int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P,
+                      const float *out, const void *dO, float *dq, float *dk, float *dv,
+                      float *dP, int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                      void *stream);
+
+/*
  * Decode with a projected key cache.  A decode step attends one new query per
  * (batch, head) to all cached keys; with the projection it needs the cached
  * K~ = K P_h (m values per key) instead of K (d values per key) ("Sparse

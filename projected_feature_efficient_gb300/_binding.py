@@ -46,6 +46,8 @@ lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
 lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
+lib.spa_attention_bwd.argtypes = [_vp] * 10 + [_i] * 8 + [_vp]
+lib.spa_attention_bwd.restype = _i
 lib.spa_topk_features.argtypes = [_vp, _vp, ctypes.c_longlong, _i, _i, _i, _vp]
 lib.spa_topk_features.restype = _i
 lib.spa_sfa_attention_fwd.argtypes = [_vp] * 4 + [_i] * 8 + [_vp]
@@ -188,6 +190,23 @@ def spa_attention_fwd_host(q, k, v, P, causal=False, out=None, stream=None):
                                       m, dv, int(bool(causal)), _dtype_code(q),
                                       _stream_ptr(stream)), "spa_attention_fwd_host")
     return out
+
+
+def spa_attention_bwd(q, k, v, P, out, dO, causal=False, stream=None):
+    """Gradients (dq, dk, dv, dP) of spa_attention_fwd for the upstream gradient
+    dO (same type as q), given the forward's fp32 output `out`."""
+    import torch
+    B, H, N, d, m, dv = _shapes(q, k, v, P)
+    dev = q.device
+    dq = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dk = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dvo = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    dP = torch.empty((H, d, m), dtype=torch.float32, device=dev)
+    _check(lib.spa_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(dO), _ptr(dq),
+                                 _ptr(dk), _ptr(dvo), _ptr(dP), B, H, N, d, m, dv,
+                                 int(bool(causal)), _dtype_code(q), _stream_ptr(stream)),
+           "spa_attention_bwd")
+    return dq, dk, dvo, dP
 
 
 def spa_topk_features(x, k, out=None, stream=None):

@@ -80,6 +80,18 @@ struct TopkParams {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream);  // P[h] = I_d
 
+// Gradients of the forward (materialised per head group, library GEMMs).
+struct BwdParams {
+  const void *q, *k, *v, *P, *dO;  // inputs (bf16 or fp32), same layouts as the forward
+  const float* out;                 // the forward's output [BH][N][dv]
+  float *dq, *dk, *dv_out, *dP;     // gradients: [BH][N][d], [BH][N][d], [BH][N][dv], [H][d][m]
+  int B, H, N, d, m, dv, causal, bf16;
+  int group;                        // heads whose N x N blocks are in memory at once
+};
+size_t backward_workspace_bytes(const BwdParams& p);
+int backward_group(int B, int H, int N, size_t budget_bytes);
+int run_backward(const BwdParams& p, void* ws, cudaStream_t stream);  // 0, -1 CUDA, -2 cuBLAS
+
 // Single-query attention against the projected key cache, split over key chunks.
 constexpr int kDecodeMaxChunk = 8192;  // keys per chunk (scores in shared memory)
 struct DecodeParams {

@@ -599,6 +599,57 @@ int spa_sfa_attention_fwd(const void* q, const void* k, const void* v, float* ou
   return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
 }
 
+int spa_attention_bwd(const void* q, const void* k, const void* v, const void* P,
+                      const float* out, const void* dO, float* dq, float* dk, float* dv,
+                      float* dP, int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                      void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) {
+    if (!dP) return SPA_ERR_NULL;  // the projection gradient is still defined: zero
+    if (H > 0 && d > 0 && m > 0 &&
+        cudaMemsetAsync(dP, 0, static_cast<size_t>(H) * d * m * sizeof(float),
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SPA_ERR_CUDA;
+    return SPA_OK;
+  }
+  if (st) return st;
+  if (d > 128) return SPA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !P || !out || !dO || !dq || !dk || !dv || !dP) return SPA_ERR_NULL;
+  spa::BwdParams bp{};
+  bp.q = q;
+  bp.k = k;
+  bp.v = v;
+  bp.P = P;
+  bp.dO = dO;
+  bp.out = out;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv_out = dv;
+  bp.dP = dP;
+  bp.B = B;
+  bp.H = H;
+  bp.N = N;
+  bp.d = d;
+  bp.m = m;
+  bp.dv = d_v;
+  bp.causal = causal != 0;
+  bp.bf16 = dtype == SPA_BF16;
+  // N x N blocks of as many heads as fit in 8 GB (at least one head)
+  bp.group = spa::backward_group(B, H, N, size_t(8) << 30);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = spa::backward_workspace_bytes(bp);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  const int rc = spa::run_backward(bp, ws, s);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (rc == -2) return SPA_ERR_CUDA;
+  if (rc) return SPA_ERR_CUDA;
+  return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
+}
+
 int spa_selftest_wait_timeout(int limit_ms) {
   if (limit_ms <= 0 || limit_ms > 2000) return SPA_ERR_SHAPE;
   constexpr int B = 1, H = 1, N = 256, d = 64, m = 32, dv = 64;
