@@ -11,6 +11,7 @@ and its fraction of the measured bf16 tensor-core peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --decode     (the decode row: projected key cache, workload D1)
+    python bench.py --backward   (the backward row, workload C3)
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent problems, no data-path collective: weak scaling); rank 0 prints
@@ -560,6 +561,114 @@ def run_decode(args, rank, world, local_rank):
     return 0
 
 
+BWD_METRIC = "projected-attention backward TFLOP/s (products of dq, dk, dv, dP)"
+
+
+def bwd_flops(B, H, N, d, m, dv, causal) -> float:
+    """FLOPs of the backward's products: the score recompute S, dA = dO V^T,
+    dQp, dKp and dV (N^2 terms halved if causal), plus the projections Qp, Kp,
+    dq, dk and the two halves of dP (2 N d m each)."""
+    n2 = 2.0 * B * H * N * N * (3 * m + 2 * dv) * (0.5 if causal else 1.0)
+    return n2 + 6 * 2.0 * B * H * N * d * m
+
+
+def bwd_bytes(B, H, N) -> float:
+    """HBM bytes of the materialised N x N blocks per backward: S written;
+    the softmax reads and writes it; dA written; dS reads A and dA and writes
+    dS; the dQp and dKp products read dS and the dV product reads A: ten fp32
+    N x N passes per head (full blocks, also with a causal mask)."""
+    return 10.0 * 4 * B * H * N * N
+
+
+def run_backward(args, rank, world, local_rank):
+    """The backward row on workload C3 (B=2 H=16 N=8192 d=128 m=32 d_v=128,
+    causal); inputs resident, the forward's output computed once beforehand."""
+    import torch
+    import torch.distributed as dist
+
+    import projected_feature_efficient_gb300 as spa
+    import spa_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = si.WORKLOADS["C3"]
+    B, H, N, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
+    q_h, k_h, v_h = si.make_qkv(w, seed=None if rank == 0 else 1000 + w.number + 7919 * rank)
+    P_h = si.make_P(w)
+    g = torch.Generator().manual_seed(3000 + rank)
+    dO_h = torch.randn((B, H, N, dv), generator=g, dtype=torch.float64).to(torch.bfloat16)
+    q, k, v, P, dO = (t.to(dev) for t in (q_h, k_h, v_h, P_h, dO_h))
+    out = spa.spa_attention_fwd(q, k, v, P, causal=w.causal)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        spa.spa_attention_bwd(q, k, v, P, out, dO, causal=w.causal)
+    barrier()
+    K = args.steps
+    sampler = ClockSampler(physical_device(local_rank))
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    barrier()
+    sampler.mark_start()
+    ev[0].record(stream)
+    for _ in range(K):
+        spa.spa_attention_bwd(q, k, v, P, out, dO, causal=w.causal)
+    ev[1].record(stream)
+    barrier()
+    sampler.mark_end()
+    clocks = sampler.summary()
+    sampler.stop()
+    t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
+    fl = bwd_flops(B, H, N, d, m, dv, w.causal)
+    value = world * fl * K / (t_ms * 1e-3) / 1e12
+    if spa.device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        hs = 1
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q_h[:1, :hs, :2048], k_h[:1, :hs, :2048], v_h[:1, :hs, :2048],
+                             P_h[:hs], dO_h[:1, :hs, :2048], causal=w.causal)
+        dt = time.perf_counter() - t0
+        cpu = {"value": bwd_flops(1, hs, 2048, d, m, dv, w.causal) / dt / 1e12, "unit": UNIT,
+               "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{hs} head, the first 2048 positions (causal), all gradients; {dt:.1f} s"}
+    if rank == 0:
+        hbm = load_hbm_peak()
+        gbs = bwd_bytes(B, H, N) / (t_ms / K * 1e-3) / 1e9
+        line = {
+            "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": t_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"C3 backward: B={B} H={H} N={N} d={d} m={m} d_v={dv} bf16 "
+                                   f"causal; upstream gradient iid N(0,1)",
+                       "B": B, "H": H, "N": N, "d": d, "m": m, "d_v": dv, "causal": True,
+                       "api": "spa_attention_bwd (forward output computed once, outside)",
+                       "parallelism": f"dp{world}"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm[0], "unit": "GB/s",
+                         "frac": gbs / hbm[0], "traffic": None,
+                         "kernel": "materialised N x N blocks (cuBLAS products + our element-wise kernels)",
+                         "peak_source": hbm[1]},
+            "gpu_launches": None,
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def load_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -588,6 +697,8 @@ def main(argv=None):
                     help="projection width of the C4 sweep")
     ap.add_argument("--decode", action="store_true",
                     help="measure the decode row (projected key cache, workload D1) instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="measure the backward row (workload C3) instead")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode with another batch size (smaller case for profiler captures)")
     args = ap.parse_args(argv)
@@ -598,6 +709,8 @@ def main(argv=None):
         return run_reference(args, rank, world)
     if args.decode:
         return run_decode(args, rank, world, local_rank)
+    if args.backward:
+        return run_backward(args, rank, world, local_rank)
     return run_ours(args, rank, world, local_rank)
 
 

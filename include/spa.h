@@ -36,6 +36,14 @@
 
 #include <stddef.h>
 
+/* Every entry point below is exported from libspa.so; the library is built
+ * with hidden visibility, so nothing else is. */
+#if defined(__GNUC__)
+#define SPA_API __attribute__((visibility("default")))
+#else
+#define SPA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -55,10 +63,10 @@ typedef enum {
 typedef enum { SPA_F32 = 0, SPA_BF16 = 1 } spa_dtype;
 
 /* Human-readable name of a status code (static storage, never NULL). */
-const char *spa_status_str(int status);
+SPA_API const char *spa_status_str(int status);
 
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
-int spa_version(void);
+SPA_API int spa_version(void);
 
 /*
  * spa_project -- the projection step alone: x_proj[b][h][i][:] = x[b][h][i][:] P_h
@@ -69,8 +77,8 @@ int spa_version(void);
  * Products of the inputs are formed exactly and summed in fp32.
  * Supported: 1 <= d <= 256, 1 <= m <= 128.
  */
-int spa_project(const void *x, const void *P, float *x_proj, int B, int H, int N, int d, int m,
-                int dtype, void *stream);
+SPA_API int spa_project(const void *x, const void *P, float *x_proj, int B, int H, int N, int d,
+                        int m, int dtype, void *stream);
 
 /*
  * spa_attention_fwd -- the whole forward: projection, scores, (causal mask),
@@ -88,16 +96,16 @@ int spa_project(const void *x, const void *P, float *x_proj, int B, int H, int N
  * cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
  * stream (SPA_ERR_NOMEM if the allocation fails).
  */
-int spa_attention_fwd(const void *q, const void *k, const void *v, const void *P, float *out,
-                      int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
-                      void *stream);
+SPA_API int spa_attention_fwd(const void *q, const void *k, const void *v, const void *P,
+                              float *out, int B, int H, int N, int d, int m, int d_v, int causal,
+                              int dtype, void *stream);
 
 /*
  * spa_attention_workspace_size -- bytes of device workspace the forward needs
  * for these sizes (0 when B*H*N == 0).  Validates like spa_attention_fwd.
  */
-int spa_attention_workspace_size(int B, int H, int N, int d, int m, int d_v, int dtype,
-                                 size_t *bytes);
+SPA_API int spa_attention_workspace_size(int B, int H, int N, int d, int m, int d_v, int dtype,
+                                         size_t *bytes);
 
 /*
  * spa_attention_fwd_ws -- spa_attention_fwd with a caller-provided workspace
@@ -105,9 +113,9 @@ int spa_attention_workspace_size(int B, int H, int N, int d, int m, int d_v, int
  * SPA_ERR_NOMEM if smaller).  The workspace is overwritten; it must not be in
  * use by other work on other streams while this call's kernels run.
  */
-int spa_attention_fwd_ws(const void *q, const void *k, const void *v, const void *P, float *out,
-                         int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
-                         void *workspace, size_t workspace_bytes, void *stream);
+SPA_API int spa_attention_fwd_ws(const void *q, const void *k, const void *v, const void *P,
+                                 float *out, int B, int H, int N, int d, int m, int d_v, int causal,
+                                 int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * spa_attention_prepare / spa_attention_apply -- the forward in two stages on
@@ -120,12 +128,12 @@ int spa_attention_fwd_ws(const void *q, const void *k, const void *v, const void
  * unchanged.  d_v must be passed to prepare as well: it takes part in the
  * size checks.
  */
-int spa_attention_prepare(const void *q, const void *k, const void *P, int B, int H, int N,
-                          int d, int m, int d_v, int dtype, void *workspace,
-                          size_t workspace_bytes, void *stream);
-int spa_attention_apply(const void *v, float *out, int B, int H, int N, int d, int m, int d_v,
-                        int causal, int dtype, const void *workspace, size_t workspace_bytes,
-                        void *stream);
+SPA_API int spa_attention_prepare(const void *q, const void *k, const void *P, int B, int H, int N,
+                                  int d, int m, int d_v, int dtype, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+SPA_API int spa_attention_apply(const void *v, float *out, int B, int H, int N, int d, int m,
+                                int d_v, int causal, int dtype, const void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * spa_attention_fwd_host -- end-to-end form on HOST buffers: copies q, k, v, P
@@ -141,9 +149,9 @@ int spa_attention_apply(const void *v, float *out, int B, int H, int N, int d, i
  * ones work but copy synchronously.  Same shapes and dtypes as
  * spa_attention_fwd.
  */
-int spa_attention_fwd_host(const void *q, const void *k, const void *v, const void *P,
-                           float *out, int B, int H, int N, int d, int m, int d_v, int causal,
-                           int dtype, void *stream);
+SPA_API int spa_attention_fwd_host(const void *q, const void *k, const void *v, const void *P,
+                                   float *out, int B, int H, int N, int d, int m, int d_v,
+                                   int causal, int dtype, void *stream);
 
 /*
  * spa_attention_fwd_noalloc -- spa_attention_fwd without any device
@@ -164,9 +172,9 @@ int spa_attention_fwd_host(const void *q, const void *k, const void *v, const vo
  *             serialise them.  Contents left by an earlier call are never read.
  *   No cudaMalloc, cudaFree or other allocating routine is called.
  */
-int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const void *P,
-                              float *out, int B, int H, int N, int d, int m, int d_v, int causal,
-                              int dtype, void *stream);
+SPA_API int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const void *P,
+                                      float *out, int B, int H, int N, int d, int m, int d_v,
+                                      int causal, int dtype, void *stream);
 
 /*
  * spa_attention_bwd -- gradients of spa_attention_fwd for an upstream gradient
@@ -184,10 +192,10 @@ int spa_attention_fwd_noalloc(const void *q, const void *k, const void *v, const
  * are the forward's.  Workspace from cudaMallocAsync on `stream`.  An empty
  * problem (B*H*N == 0) zeroes dP.
  */
-int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P,
-                      const float *out, const void *dO, float *dq, float *dk, float *dv,
-                      float *dP, int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
-                      void *stream);
+SPA_API int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P,
+                              const float *out, const void *dO, float *dq, float *dk, float *dv,
+                              float *dP, int B, int H, int N, int d, int m, int d_v, int causal,
+                              int dtype, void *stream);
 
 /*
  * Decode with a projected key cache.  A decode step attends one new query per
@@ -216,11 +224,11 @@ int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P
  *   q~ (B*H*m floats) are taken with cudaMallocAsync on `stream` and released.  Equivalent to the
  *   last row of the causal forward over the same L keys.
  */
-int spa_kcache_append(const void *k, const void *P, void *kc, float *kc_mul, int B, int H, int T,
-                      int d, int m, int pos, int cap, int dtype, void *stream);
-int spa_attention_decode(const void *q, const void *P, const void *kc, const float *kc_mul,
-                         const void *v, float *out, int B, int H, int L, int d, int m, int d_v,
-                         int cap, int dtype, void *stream);
+SPA_API int spa_kcache_append(const void *k, const void *P, void *kc, float *kc_mul, int B, int H,
+                              int T, int d, int m, int pos, int cap, int dtype, void *stream);
+SPA_API int spa_attention_decode(const void *q, const void *P, const void *kc, const float *kc_mul,
+                                 const void *v, float *out, int B, int H, int L, int d, int m,
+                                 int d_v, int cap, int dtype, void *stream);
 
 /*
  * Sparse Feature Attention ("Scaling Attention via Feature Sparsity" notes,
@@ -241,10 +249,11 @@ int spa_attention_decode(const void *q, const void *P, const void *kc, const flo
  *   {32, 64, 128}.  The sparsified copies, the identity P and the workspace
  *   are taken with cudaMallocAsync on `stream` and released.
  */
-int spa_topk_features(const void *x, void *y, long long rows, int d, int k, int dtype,
-                      void *stream);
-int spa_sfa_attention_fwd(const void *q, const void *k, const void *v, float *out, int B, int H,
-                          int N, int d, int d_v, int topk, int causal, int dtype, void *stream);
+SPA_API int spa_topk_features(const void *x, void *y, long long rows, int d, int k, int dtype,
+                              void *stream);
+SPA_API int spa_sfa_attention_fwd(const void *q, const void *k, const void *v, float *out, int B,
+                                  int H, int N, int d, int d_v, int topk, int causal, int dtype,
+                                  void *stream);
 
 /*
  * spa_selftest_wait_timeout -- failure-detection self-test (the pages have no
@@ -260,14 +269,14 @@ int spa_sfa_attention_fwd(const void *q, const void *k, const void *v, float *ou
  * outcome), SPA_OK when it was not, or another status if a call failed.  The
  * device stays usable afterwards.
  */
-int spa_selftest_wait_timeout(int limit_ms);
+SPA_API int spa_selftest_wait_timeout(int limit_ms);
 
 /*
  * spa_device_error -- reads and clears the device error word of the current
  * device (synchronising it first).  *code receives 0 when no kernel gave up
  * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.
  */
-int spa_device_error(int *code);
+SPA_API int spa_device_error(int *code);
 
 #ifdef __cplusplus
 }

@@ -50,7 +50,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         return LIB
     nvcc = nvcc_path()
     os.makedirs(BUILD, exist_ok=True)
-    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                     "-I", os.path.join(ROOT, "include"), *extra_flags]
     if verbose:
         flags += ["-Xptxas", "-v"]

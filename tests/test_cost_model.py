@@ -77,3 +77,10 @@ def test_decode_bytes_per_step():
     assert bench.decode_bytes(8, 32, 32768, 32, 128) == 8 * 32 * 32768 * 324
     ratio = bench.decode_bytes(1, 1, 1, 32, 128) / (2 * 128 + 2 * 128)
     assert abs(ratio - 0.6328125) < 1e-12
+
+
+def test_backward_flop_and_byte_models():
+    # per head and N^2 term: S (2m), dA (2 d_v), dQp (2m), dKp (2m), dV (2 d_v)
+    assert bench.bwd_flops(1, 1, 10, 4, 3, 5, False) == 2 * 100 * (9 + 10) + 12 * 10 * 4 * 3
+    assert bench.bwd_flops(1, 1, 10, 4, 3, 5, True) == 100 * (9 + 10) + 12 * 10 * 4 * 3
+    assert bench.bwd_bytes(2, 16, 8192) == 10 * 4 * 32 * 8192 * 8192
