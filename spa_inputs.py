@@ -99,6 +99,21 @@ def make_qkv(w: Workload, seed: int | None = None, device="cpu"):
     return (q.to(dt).to(device), k.to(dt).to(device), v.to(dt).to(device))
 
 
+def make_sparse_P(w: Workload, s: float, seed: int, device="cpu"):
+    """Per-head projection drawn as the sparse random matrix of SPA Definition
+    1 (Sec. 2.2): every entry is sqrt(s/m) times +1 with probability 1/(2s),
+    -1 with probability 1/(2s), and 0 otherwise (s >= 1).  Drawn in fp64 from a
+    seeded uniform, then cast to the workload dtype."""
+    assert s >= 1
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    u = torch.rand((w.H, w.d, w.m), generator=g, dtype=torch.float64)
+    sign = torch.zeros_like(u)
+    sign[u < 0.5 / s] = 1.0
+    sign[u >= 1.0 - 0.5 / s] = -1.0
+    return (sign * math.sqrt(s / w.m)).to(w.torch_dtype).to(device)
+
+
 def make_P(w: Workload, seed: int | None = None, device="cpu"):
     """Per-head projection P [H,d,m], entries N(0, 1/m), or the identity."""
     dt = w.torch_dtype
