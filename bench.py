@@ -572,17 +572,18 @@ def bwd_flops(B, H, N, d, m, dv, causal) -> float:
     return n2 + 6 * 2.0 * B * H * N * d * m
 
 
-def bwd_bytes(B, H, N) -> float:
-    """HBM bytes of the materialised N x N blocks per backward: S written;
-    the softmax reads and writes it; dA written; dS reads A and dA and writes
-    dS; the dQp and dKp products read dS and the dV product reads A: ten fp32
-    N x N passes per head (full blocks, also with a causal mask)."""
-    return 10.0 * 4 * B * H * N * N
+def bwd_kernel_flops(B, H, N, m, dv, causal) -> float:
+    """Algorithmic FLOPs of one fused backward kernel launch: the score
+    recompute S, dA = dO V^T, dV, dQp and dKp (N^2 terms, halved if causal)."""
+    return 2.0 * B * H * N * N * (3 * m + 2 * dv) * (0.5 if causal else 1.0)
 
 
 def run_backward(args, rank, world, local_rank):
     """The backward row on workload C3 (B=2 H=16 N=8192 d=128 m=32 d_v=128,
-    causal); inputs resident, the forward's output computed once beforehand."""
+    causal); inputs resident; the forward's output and row log-sum-exp are
+    computed once beforehand (spa_attention_fwd_lse).  A step is the fused
+    backward in its three stages (prepare, the tensor-core kernel, finish);
+    the kernel is also timed alone for the roofline."""
     import torch
     import torch.distributed as dist
 
@@ -600,32 +601,51 @@ def run_backward(args, rank, world, local_rank):
     g = torch.Generator().manual_seed(3000 + rank)
     dO_h = torch.randn((B, H, N, dv), generator=g, dtype=torch.float64).to(torch.bfloat16)
     q, k, v, P, dO = (t.to(dev) for t in (q_h, k_h, v_h, P_h, dO_h))
-    out = spa.spa_attention_fwd(q, k, v, P, causal=w.causal)
+    out, lse = spa.spa_attention_fwd_lse(q, k, v, P, causal=w.causal)
+    ws = torch.empty(spa.spa_attention_bwd_workspace_size(B, H, N, d, m, dv, spa.SPA_BF16),
+                     dtype=torch.uint8, device=dev)
+    dq = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dk = torch.empty_like(dq)
+    dvo = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    dP = torch.empty((H, d, m), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def step():
+        spa.spa_attention_bwd_prepare(q, k, P, out, lse, dO, ws)
+        spa.spa_attention_bwd_apply(v, dO, dvo, ws, B, H, N, d, m, causal=w.causal)
+        spa.spa_attention_bwd_finish(q, k, P, dq, dk, dP, dv, ws)
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(max(3, args.warmup)):
-        spa.spa_attention_bwd(q, k, v, P, out, dO, causal=w.causal)
+    W = max(3, args.warmup)
+    for _ in range(W):
+        step()
     barrier()
     K = args.steps
     sampler = ClockSampler(physical_device(local_rank))
     time.sleep(0.3)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     barrier()
     sampler.mark_start()
     ev[0].record(stream)
     for _ in range(K):
-        spa.spa_attention_bwd(q, k, v, P, out, dO, causal=w.causal)
+        step()
     ev[1].record(stream)
+    barrier()
+    # the tensor-core kernel alone (same inputs; the dQp accumulator keeps adding)
+    ev[2].record(stream)
+    for _ in range(K):
+        spa.spa_attention_bwd_apply(v, dO, dvo, ws, B, H, N, d, m, causal=w.causal)
+    ev[3].record(stream)
     barrier()
     sampler.mark_end()
     clocks = sampler.summary()
     sampler.stop()
     t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
+    k_ms = ev[2].elapsed_time(ev[3]) / K
     fl = bwd_flops(B, H, N, d, m, dv, w.causal)
     value = world * fl * K / (t_ms * 1e-3) / 1e12
     if spa.device_error() != 0:
@@ -642,22 +662,26 @@ def run_backward(args, rank, world, local_rank):
                "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{hs} head, the first 2048 positions (causal), all gradients; {dt:.1f} s"}
     if rank == 0:
-        hbm = load_hbm_peak()
-        gbs = bwd_bytes(B, H, N) / (t_ms / K * 1e-3) / 1e9
+        peak, peak_sus, peak_src = load_peaks()
+        achieved = bwd_kernel_flops(B, H, N, m, dv, w.causal) / (k_ms * 1e-3) / 1e12
         line = {
             "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": t_ms / K, "higher_is_better": True,
+            "warmup": W, "ms_per_step": t_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"C3 backward: B={B} H={H} N={N} d={d} m={m} d_v={dv} bf16 "
                                    f"causal; upstream gradient iid N(0,1)",
                        "B": B, "H": H, "N": N, "d": d, "m": m, "d_v": dv, "causal": True,
-                       "api": "spa_attention_bwd (forward output computed once, outside)",
+                       "api": "spa_attention_bwd_prepare / _apply / _finish (forward output "
+                              "and lse computed once, outside)",
+                       "l2": "inputs and workspace (q, k, v, dO, 207 MB workspace) exceed L2",
                        "parallelism": f"dp{world}"},
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm[0], "unit": "GB/s",
-                         "frac": gbs / hbm[0], "traffic": None,
-                         "kernel": "materialised N x N blocks (cuBLAS products + our element-wise kernels)",
-                         "peak_source": hbm[1]},
-            "gpu_launches": None,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "kernel": "bwd_ws_kernel (S, dP, dV, dKp, dQp on tcgen05)",
+                         "peak_source": f"{peak_src} bf16 burst",
+                         "frac_of_sustained": achieved / peak_sus},
+            "kernels_ms_per_step": {"bwd_ws_kernel": k_ms, "rest": t_ms / K - k_ms},
+            "gpu_launches": 7 * K,
             "clocks": clocks,
         }
         if cpu is not None:

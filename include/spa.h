@@ -177,6 +177,19 @@ SPA_API int spa_attention_fwd_noalloc(const void *q, const void *k, const void *
                                       int causal, int dtype, void *stream);
 
 /*
+ * spa_attention_fwd_lse -- spa_attention_fwd that also writes, for every query
+ * row, the log-sum-exp of its logits (natural log):
+ *   lse[b][h][i] = log sum_{j visible} exp(<Qp_i, Kp_j> / sqrt(m))
+ * lse is [B][H][N] fp32, device, 4-byte aligned.  It is what
+ * spa_attention_bwd_lse needs to recompute the probabilities A_ij =
+ * exp(s_ij - lse_i) without a second forward.  Limits and workspace as
+ * spa_attention_fwd.
+ */
+SPA_API int spa_attention_fwd_lse(const void *q, const void *k, const void *v, const void *P,
+                                  float *out, float *lse, int B, int H, int N, int d, int m,
+                                  int d_v, int causal, int dtype, void *stream);
+
+/*
  * spa_attention_bwd -- gradients of spa_attention_fwd for an upstream gradient
  * dO [B][H][N][d_v] (same type as the inputs), given the forward's output out
  * (fp32).  Writes dq, dk [B][H][N][d], dv [B][H][N][d_v] and dP [H][d][m] (the
@@ -185,17 +198,59 @@ SPA_API int spa_attention_fwd_noalloc(const void *q, const void *k, const void *
  *   dS = A * (dO V^T - D) / sqrt(m), dQp = dS Kp, dKp = dS^T Qp, dV = A^T dO,
  *   dq = dQp P_h^T, dk = dKp P_h^T, dP_h = sum_b (q^T dQp + k^T dKp)
  * ("Sparse Projection Attention", Sec. 3.4.1; Algorithm 2 trains P through
- * these).  This version materialises A and dS for as many heads as fit in
- * 8 GB at a time (2 N^2 floats per head) and uses cuBLAS for the plain
- * products (fp32 accumulation; TF32 products for bf16 inputs, exact for
- * their values; fp32 products for fp32 inputs).  d <= 128; the other limits
- * are the forward's.  Workspace from cudaMallocAsync on `stream`.  An empty
- * problem (B*H*N == 0) zeroes dP.
+ * these).  d <= 128; the other limits are the forward's.  Two implementations:
+ *   fused (SPA_BF16, m in {16, 32}, d_v in {64, 128}; every pointer 16-byte
+ *     aligned, else SPA_ERR_ALIGN): A and dS are recomputed tile by tile on
+ *     the tensor cores from the forward's row log-sum-exp and never stored.
+ *     The scores use the forward's own operands; P^T and dS are rounded to
+ *     bf16 for their products (fp32 accumulation), dQp / dKp are carried
+ *     into dq, dk, dP as bf16 hi + lo pairs.  spa_attention_bwd runs the
+ *     forward once more for the log-sum-exp; spa_attention_bwd_lse takes it.
+ *   materialised (other cases): A and dS for as many heads as fit in 8 GB at
+ *     a time (2 N^2 floats per head), plain cuBLAS products (fp32
+ *     accumulation; TF32 products for bf16 inputs, exact for their values;
+ *     fp32 products for fp32 inputs).
+ * Workspace from cudaMallocAsync on `stream`.  An empty problem (B*H*N == 0)
+ * zeroes dP.
  */
 SPA_API int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P,
                               const float *out, const void *dO, float *dq, float *dk, float *dv,
                               float *dP, int B, int H, int N, int d, int m, int d_v, int causal,
                               int dtype, void *stream);
+/* spa_attention_bwd_lse -- the same with the forward's lse ([B][H][N] fp32, as
+ * written by spa_attention_fwd_lse; SPA_ERR_NULL if missing), so the fused
+ * path skips its own forward.  The materialised path ignores lse. */
+SPA_API int spa_attention_bwd_lse(const void *q, const void *k, const void *v, const void *P,
+                                  const float *out, const float *lse, const void *dO, float *dq,
+                                  float *dk, float *dv, float *dP, int B, int H, int N, int d,
+                                  int m, int d_v, int causal, int dtype, void *stream);
+
+/*
+ * The fused backward in three stages on a caller-provided workspace (device,
+ * 256-byte aligned, at least spa_attention_bwd_workspace_size() bytes; the
+ * stages must run in order on one stream with the same sizes and workspace).
+ * Fused shapes only (SPA_BF16, d <= 128, m in {16, 32}, d_v in {64, 128};
+ * otherwise SPA_ERR_UNSUPPORTED); pointers 16-byte aligned.
+ *   prepare: the forward's score operands, bf16 Qp / Kp tiles, row statistics
+ *            (D_i = <dO_i, out_i>, lse) and a zeroed dQp accumulator.
+ *   apply:   the tensor-core kernel; writes dv and leaves dQp, dKp in the
+ *            workspace.
+ *   finish:  dq, dk, dP from dQp, dKp (library GEMMs).
+ * prepare + apply + finish gives exactly spa_attention_bwd_lse.
+ */
+SPA_API int spa_attention_bwd_workspace_size(int B, int H, int N, int d, int m, int d_v,
+                                             int dtype, size_t *bytes);
+SPA_API int spa_attention_bwd_prepare(const void *q, const void *k, const void *P,
+                                      const float *out, const float *lse, const void *dO, int B,
+                                      int H, int N, int d, int m, int d_v, int dtype,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+SPA_API int spa_attention_bwd_apply(const void *v, const void *dO, float *dv, int B, int H, int N,
+                                    int d, int m, int d_v, int causal, int dtype, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+SPA_API int spa_attention_bwd_finish(const void *q, const void *k, const void *P, float *dq,
+                                     float *dk, float *dP, int B, int H, int N, int d, int m,
+                                     int d_v, int dtype, void *workspace, size_t workspace_bytes,
+                                     void *stream);
 
 /*
  * Decode with a projected key cache.  A decode step attends one new query per

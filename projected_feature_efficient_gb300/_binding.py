@@ -48,6 +48,18 @@ lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
 lib.spa_attention_bwd.argtypes = [_vp] * 10 + [_i] * 8 + [_vp]
 lib.spa_attention_bwd.restype = _i
+lib.spa_attention_bwd_lse.argtypes = [_vp] * 11 + [_i] * 8 + [_vp]
+lib.spa_attention_bwd_lse.restype = _i
+lib.spa_attention_fwd_lse.argtypes = [_vp] * 6 + [_i] * 8 + [_vp]
+lib.spa_attention_fwd_lse.restype = _i
+lib.spa_attention_bwd_workspace_size.argtypes = [_i] * 7 + [ctypes.POINTER(_sz)]
+lib.spa_attention_bwd_workspace_size.restype = _i
+lib.spa_attention_bwd_prepare.argtypes = [_vp] * 6 + [_i] * 7 + [_vp, _sz, _vp]
+lib.spa_attention_bwd_prepare.restype = _i
+lib.spa_attention_bwd_apply.argtypes = [_vp] * 3 + [_i] * 8 + [_vp, _sz, _vp]
+lib.spa_attention_bwd_apply.restype = _i
+lib.spa_attention_bwd_finish.argtypes = [_vp] * 6 + [_i] * 7 + [_vp, _sz, _vp]
+lib.spa_attention_bwd_finish.restype = _i
 lib.spa_topk_features.argtypes = [_vp, _vp, ctypes.c_longlong, _i, _i, _i, _vp]
 lib.spa_topk_features.restype = _i
 lib.spa_sfa_attention_fwd.argtypes = [_vp] * 4 + [_i] * 8 + [_vp]
@@ -207,6 +219,76 @@ def spa_attention_bwd(q, k, v, P, out, dO, causal=False, stream=None):
                                  int(bool(causal)), _dtype_code(q), _stream_ptr(stream)),
            "spa_attention_bwd")
     return dq, dk, dvo, dP
+
+
+def spa_attention_fwd_lse(q, k, v, P, causal=False, out=None, lse=None, stream=None):
+    """Forward that also returns the row log-sum-exp of the logits: (out, lse),
+    out fp32 [B,H,N,dv], lse fp32 [B,H,N]."""
+    import torch
+    B, H, N, d, m, dv = _shapes(q, k, v, P)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(lib.spa_attention_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), B,
+                                     H, N, d, m, dv, int(bool(causal)), _dtype_code(q),
+                                     _stream_ptr(stream)), "spa_attention_fwd_lse")
+    return out, lse
+
+
+def spa_attention_bwd_lse(q, k, v, P, out, lse, dO, causal=False, grads=None, stream=None):
+    """Gradients (dq, dk, dv, dP) given the forward's output and row log-sum-exp
+    (from spa_attention_fwd_lse).  `grads` may supply the four fp32 output tensors."""
+    import torch
+    B, H, N, d, m, dv = _shapes(q, k, v, P)
+    dev = q.device
+    if grads is None:
+        grads = (torch.empty((B, H, N, d), dtype=torch.float32, device=dev),
+                 torch.empty((B, H, N, d), dtype=torch.float32, device=dev),
+                 torch.empty((B, H, N, dv), dtype=torch.float32, device=dev),
+                 torch.empty((H, d, m), dtype=torch.float32, device=dev))
+    dq, dk, dvo, dP = grads
+    _check(lib.spa_attention_bwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse),
+                                     _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dvo), _ptr(dP), B, H, N, d,
+                                     m, dv, int(bool(causal)), _dtype_code(q),
+                                     _stream_ptr(stream)), "spa_attention_bwd_lse")
+    return dq, dk, dvo, dP
+
+
+def spa_attention_bwd_workspace_size(B, H, N, d, m, dv, dtype_code) -> int:
+    n = _sz(0)
+    _check(lib.spa_attention_bwd_workspace_size(B, H, N, d, m, dv, dtype_code, ctypes.byref(n)),
+           "spa_attention_bwd_workspace_size")
+    return int(n.value)
+
+
+def spa_attention_bwd_prepare(q, k, P, out, lse, dO, workspace, stream=None):
+    """Fused backward stage 1 into `workspace` (uint8 device tensor)."""
+    B, H, N, d = q.shape
+    m, dv = P.shape[-1], dO.shape[-1]
+    _check(lib.spa_attention_bwd_prepare(_ptr(q), _ptr(k), _ptr(P), _ptr(out), _ptr(lse), _ptr(dO),
+                                         B, H, N, d, m, dv, _dtype_code(q), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_ptr(stream)), "spa_attention_bwd_prepare")
+
+
+def spa_attention_bwd_apply(v, dO, dv_out, workspace, B, H, N, d, m, causal=False, stream=None):
+    """Fused backward stage 2: the tensor-core kernel; writes dv_out (fp32)."""
+    dv = v.shape[-1]
+    _check(lib.spa_attention_bwd_apply(_ptr(v), _ptr(dO), _ptr(dv_out), B, H, N, d, m, dv,
+                                       int(bool(causal)), _dtype_code(v), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream_ptr(stream)), "spa_attention_bwd_apply")
+
+
+def spa_attention_bwd_finish(q, k, P, dq, dk, dP, dv, workspace, stream=None):
+    """Fused backward stage 3: dq, dk, dP (fp32) from the workspace; dv = d_v."""
+    B, H, N, d = q.shape
+    m = P.shape[-1]
+    _check(lib.spa_attention_bwd_finish(_ptr(q), _ptr(k), _ptr(P), _ptr(dq), _ptr(dk), _ptr(dP), B,
+                                        H, N, d, m, int(dv), _dtype_code(q), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream_ptr(stream)), "spa_attention_bwd_finish")
 
 
 def spa_topk_features(x, k, out=None, stream=None):

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const AttnF32Para
   }
   float* dst = p.out + (static_cast<size_t>(bh) * p.N + i) * p.dv;
   const float inv = 1.f / l_run;
+  if (p.lse != nullptr && lane == 0) p.lse[static_cast<size_t>(bh) * p.N + i] = m_run + logf(l_run);
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const int col = lane + 32 * c;

@@ -42,6 +42,10 @@
 // same relative precision), which leaves the final O / l unchanged up to
 // rounding and skips almost every rescale of O.
 //
+// With an `lse` buffer the output step also writes each row's log-sum-exp
+// (m + log2 l, converted to natural log), which the fused backward uses to
+// recompute the probabilities.
+//
 // Every wait is bounded (2 s).  A role that gives up sets the CTA abort flag
 // and the device error word; every role leaves its loop, the MMA issuer and
 // the loader wait (bounded) for their own operations in flight, the TMA stores
@@ -50,6 +54,7 @@
 
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "waits.cuh"
 
 namespace spa {
 namespace {
@@ -72,6 +77,7 @@ struct RegSplit {
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 20.f;  // log2 units: p <= 2^20 between rescales
+constexpr float kLn2 = 0.693147180559945309f;
 constexpr int kBoxBytes = kTileRows * 128;  // one 128-row x 128-byte output box
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;  // per-block limit less the static part
 
@@ -103,25 +109,6 @@ struct Bars {
   uint64_t drain;
 };
 
-// What a bounded wait needs: the CTA's abort flag, the device error word and
-// the time limit of one wait.
-struct WaitCtl {
-  volatile int* abort;
-  int* err;
-  uint64_t limit_ns;
-};
-
-// Bounded wait that also gives up once another role of the CTA has aborted.
-// The common case (phase already complete) costs one try_wait.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  if (*ctl.abort) return false;
-  if (mbar_wait(bar, parity, ctl.limit_ns)) return true;
-  *ctl.abort = 1;
-  atomicExch(ctl.err, 1);
-  return false;
-}
-
 // Work item -> (head, query-tile pair) and the key-tile counts of its tiles.
 struct Item {
   int bh, qt0, nkv0, nkv1, nkv;
@@ -141,15 +128,6 @@ __device__ __forceinline__ Item decode_item(const AttnTcParams& p, int w) {
   it.nkv = max(it.nkv0, it.nkv1);
   return it;
 }
-// The k-th item of this CTA: rounds of gridDim.x items, every other round in
-// reverse, so that a CTA that drew a longer item in one round draws a shorter
-// one in the next.  Returns -1 past the end.
-__device__ __forceinline__ int item_index(int k, int items) {
-  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const int w = k * G + ((k & 1) ? G - 1 - c : c);
-  return w < items ? w : -1;
-}
-
 // ---------------------------------------------------------------- loader
 // The loader role (one thread): per item the Qp tiles of its query-tile pair,
 // then the item's key tiles through the ring of Plan::kStages slots, each slot
@@ -527,6 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv = 1.f / l_run;
+      if (p.lse != nullptr) {  // log-sum-exp of the row's logits, natural log
+        const int row = qt * kTileRows + r;
+        if (row < p.N) p.lse[static_cast<size_t>(it.bh) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
+      }
       write_out_tile<DV, Plan::kBoxesPerTile>(
           tO, sbase + Plan::kStage + t * Plan::kBoxesPerTile * kBoxBytes, r, lane, inv, &omap, qt,
           it.bh, bar_id, &bars.o_empty[t]);

@@ -7,13 +7,15 @@
 //   dQp = dS Kp,    dKp = dS^T Qp
 //   dQ  = dQp P_h^T,  dK = dKp P_h^T,  dP_h = sum_b (Q^T dQp + K^T dKp)
 //
-// This version materialises A and dS for a group of heads at a time: the
+// This file holds the general version (fp32 inputs, and shapes the fused
+// tensor-core backward in bwd_ws.cu does not cover).  It materialises A and dS
+// for a group of heads at a time: the
 // products are plain library GEMMs (cuBLAS, fp32 accumulation; TF32 products
 // for bf16 inputs, whose values TF32 holds exactly; full fp32 for fp32
 // inputs) and the element-wise steps (conversion, the row dot D, the masked
 // softmax, dS, the batch sum of dP) are the kernels below.  It is HBM-bound on
-// the N x N blocks; a fused tensor-core backward that streams them is the
-// next step.
+// the N x N blocks.  The file also holds the library products that turn the
+// fused backward's dQp / dKp into dq, dk and dP (run_backward_post).
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -102,8 +104,27 @@ cublasStatus_t gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, 
                                     &beta, C, CUDA_R_32F, ldc, sC, batch, ct, CUBLAS_GEMM_DEFAULT);
 }
 
+// The same with bf16 A and B (fp32 accumulation and output).
+cublasStatus_t gemm_rm_bf16(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, const void* A,
+                            int lda, long long sA, const void* B, int ldb, long long sB, float* C,
+                            int ldc, long long sC, int batch, float alpha, float beta) {
+  return cublasGemmStridedBatchedEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N,
+                                    N, M, K, &alpha, B, CUDA_R_16BF, ldb, sB, A, CUDA_R_16BF, lda, sA,
+                                    &beta, C, CUDA_R_32F, ldc, sC, batch, CUBLAS_COMPUTE_32F,
+                                    CUBLAS_GEMM_DEFAULT);
+}
+
 std::mutex g_blas_mutex;
 cublasHandle_t g_blas[64] = {};
+
+// The device's handle, bound to `stream`; the caller holds g_blas_mutex.
+cublasHandle_t blas_handle(cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) return nullptr;
+  if (cublasSetStream(g_blas[dev], stream) != CUBLAS_STATUS_SUCCESS) return nullptr;
+  return g_blas[dev];
+}
 
 }  // namespace
 
@@ -131,12 +152,9 @@ int backward_group(int B, int H, int N, size_t budget_bytes) {
 
 // Returns 0, or -1 for a CUDA error, -2 for a cuBLAS error.
 int run_backward(const BwdParams& p, void* ws, cudaStream_t stream) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::lock_guard<std::mutex> lock(g_blas_mutex);  // one handle per device, one user at a time
-  if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) return -2;
-  cublasHandle_t h = g_blas[dev];
-  if (cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return -2;
+  cublasHandle_t h = blas_handle(stream);
+  if (!h) return -2;
   const cublasComputeType_t ct = p.bf16 ? CUBLAS_COMPUTE_32F_FAST_TF32 : CUBLAS_COMPUTE_32F;
 
   const long long BH = static_cast<long long>(p.B) * p.H, N = p.N;
@@ -222,6 +240,41 @@ int run_backward(const BwdParams& p, void* ws, cudaStream_t stream) {
       return -2;
   }
   return 0;
+}
+
+// The projection's share of the fused backward.  xq, xk hold dQp and dKp as
+// bf16 pairs [hi | lo] per row ([BH][N][2m]; hi + lo carries 16 significant
+// bits), P2[h] = [P_h | P_h] ([H][d][2m]), so that
+//   dq = xq P2^T = dQp P_h^T,   dk = xk P2^T = dKp P_h^T,
+//   R_h = sum_b q^T xq + k^T xk  ([H][d][2m]),  dP_h = R_h[:, :m] + R_h[:, m:].
+// Every product is a plain bf16 GEMM with fp32 accumulation.
+int run_backward_post(const void* q, const void* k, const uint16_t* P2, const uint16_t* xq,
+                      const uint16_t* xk, float* R, float* dq, float* dk, float* dP, int B,
+                      int H, int N, int d, int m, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_blas_mutex);
+  cublasHandle_t h = blas_handle(stream);
+  if (!h) return -2;
+  const long long Nl = N, m2 = 2 * m;
+  const auto* qb = static_cast<const uint16_t*>(q);
+  const auto* kb = static_cast<const uint16_t*>(k);
+  for (int b = 0; b < B; ++b) {
+    const long long o = static_cast<long long>(b) * H * Nl;
+    if (gemm_rm_bf16(h, false, true, N, d, static_cast<int>(m2), xq + o * m2, static_cast<int>(m2),
+                     Nl * m2, P2, static_cast<int>(m2), static_cast<long long>(d) * m2, dq + o * d, d,
+                     Nl * d, H, 1.f, 0.f) != CUBLAS_STATUS_SUCCESS ||
+        gemm_rm_bf16(h, false, true, N, d, static_cast<int>(m2), xk + o * m2, static_cast<int>(m2),
+                     Nl * m2, P2, static_cast<int>(m2), static_cast<long long>(d) * m2, dk + o * d, d,
+                     Nl * d, H, 1.f, 0.f) != CUBLAS_STATUS_SUCCESS ||
+        gemm_rm_bf16(h, true, false, d, static_cast<int>(m2), N, qb + o * d, d, Nl * d, xq + o * m2,
+                     static_cast<int>(m2), Nl * m2, R, static_cast<int>(m2),
+                     static_cast<long long>(d) * m2, H, 1.f, b == 0 ? 0.f : 1.f) !=
+            CUBLAS_STATUS_SUCCESS ||
+        gemm_rm_bf16(h, true, false, d, static_cast<int>(m2), N, kb + o * d, d, Nl * d, xk + o * m2,
+                     static_cast<int>(m2), Nl * m2, R, static_cast<int>(m2),
+                     static_cast<long long>(d) * m2, H, 1.f, 1.f) != CUBLAS_STATUS_SUCCESS)
+      return -2;
+  }
+  return launch_bwd_fold(R, dP, H, d, m, stream) == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace spa

@@ -1,0 +1,756 @@
+// bwd_ws.cu -- fused backward of projected-feature attention on tcgen05
+// ("Sparse Projection Attention", Sec. 3.4.1: P_h is trained through the
+// gradients of the attention; Algorithm 2 updates it from them).
+//
+// Per (batch, head), with the logits s_ij = <Qp_i, Kp_j> / sqrt(m), the
+// forward's row log-sum-exp L_i and D_i = <dO_i, O_i>:
+//   A_ij = exp(s_ij - L_i)                      (recomputed, never stored)
+//   dV   = A^T dO
+//   dS   = A * (dO V^T - D) / sqrt(m)           (gradient of Qp Kp^T)
+//   dQp  = dS Kp,   dKp = dS^T Qp
+// No N x N block is written to memory.  A work item is one 128-row key tile
+// of one head; its CTA walks the query tiles that see it (all of them, or
+// those on and below the diagonal with the causal mask), keeps dV and dKp of
+// its key rows in tensor memory, and adds each query tile's share of dQp into
+// an fp32 accumulator in global memory with a bulk reduce-add.
+//
+// Sixteen warps in four warpgroups:
+//   warps 0-7    gradient warpgroups.  TMEM lane = key row of the item's tile;
+//                warpgroup g takes query columns 64g .. 64g+63.
+//                  P-phase:  S^T -> P^T = exp2(S^T a_i - L_i log2 e), a_i the
+//                            range multipliers of the score operands; bf16 P^T
+//                            written over its own S^T columns for the dV product.
+//                  dS-phase: dP^T -> dS^T = P^T (dP^T / sqrt(m) - D_i / sqrt(m));
+//                            bf16 dS^T written over its own dP^T columns (dKp
+//                            product) and into a shared-memory tile in the
+//                            MN-major layout the dQp product reads (dS, M = queries).
+//   warps 8-11   epilogue: per query tile the column factors a_i, then the
+//                dQp tile out of TMEM, through a staging tile, into the
+//                reduce-add; per item the dV and dKp rows.
+//   warp 12      loads (one thread): per item the key tile's score operand,
+//                its bf16 Kp tile and V; per query tile a two-slot ring of
+//                dO, the score operand, the bf16 Qp tile and the row statistics.
+//   warp 13      tensor-memory allocation and tcgen05.mma issue (one thread).
+//   warps 14-15  idle.
+// Tensor memory (512 columns): S^T/P^T | dP^T/dS^T | dV | dKp | dQp.
+// MMA issue order per query tile i:
+//   S^T(i) = Kf Qf_i^T      (first tile of an item only; otherwise issued early)
+//   dP^T(i) = V dO_i^T
+//   dV += P^T(i) dO_i        (A from TMEM)               after the P-phase
+//   S^T(i+1)                 (overwrites P^T(i) after the dV product read it)
+//   dKp += dS^T(i) Qb_i      (A from TMEM)               after the dS-phase
+//   dQp_i = dS(i) Kb         (A from shared memory)
+// so the P-phase of tile i+1 overlaps the dKp/dQp/dP products, and the
+// dS-phase of tile i overlaps the dV and next score products.  MMAs from one
+// thread execute in issue order, so an MMA that overwrites columns never
+// overtakes an earlier one reading them.
+//
+// Every wait is bounded; a role that gives up sets the CTA abort flag and the
+// device error word, every role leaves its loop, the issuer and the loader
+// wait (bounded) for their own operations in flight, the bulk reduce-adds
+// finish reading shared memory, and TMEM is freed before the CTA exits.
+#include <math.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "waits.cuh"
+
+namespace spa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBThreads = 512;
+constexpr int kBLoadWarp = 12;
+constexpr int kBMmaWarp = 13;
+constexpr int kBMaxDynSmem = 227 * 1024 - 1024;
+constexpr uint32_t kEpiBar = 1;  // named barrier of the epilogue warpgroup
+
+template <int KD, int MB, int DV>
+struct BwdPlan {
+  static constexpr int kKfBytes = kTileRows * KD * 2;   // score-operand tile
+  static constexpr int kBBytes = kTileRows * MB * 2;    // bf16 Qp / Kp tile
+  static constexpr int kVBytes = kTileRows * DV * 2;    // V or dO tile (64-column SW128 boxes)
+  static constexpr int kStatBytes = 4 * kTileRows * 4;  // planes: qm, nl, dn, a
+  static constexpr int kDsBytes = kTileRows * kTileRows * 2;
+  static constexpr int kDqBytes = kTileRows * MB * 4;
+  // ring stage: dO | Qf | Qb | stats, padded so every dO tile is 1024-aligned
+  static constexpr int kStDo = 0;
+  static constexpr int kStQf = kVBytes;
+  static constexpr int kStQb = kStQf + kKfBytes;
+  static constexpr int kStStat = kStQb + kBBytes;
+  static constexpr int kStageBytes = (kStStat + kStatBytes + 1023) / 1024 * 1024;
+  static constexpr int kV = 0;
+  static constexpr int kDs = kV + kVBytes;
+  static constexpr int kRing = kDs + kDsBytes;
+  static constexpr int kKf = kRing + 2 * kStageBytes;
+  static constexpr int kKb = kKf + kKfBytes;
+  static constexpr int kDq = kKb + kBBytes;
+  static constexpr int kBytes = kDq + kDqBytes;
+  static constexpr int kLaunch = kBytes + 1024;  // room to align the base to 1024
+  static_assert(kLaunch <= kBMaxDynSmem, "backward shared-memory plan too large");
+  static_assert(kVBytes % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024 alignment");
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + DV,
+                            kColDQ = 256 + DV + MB;
+  static_assert(kColDQ + MB <= 512, "tensor-memory plan too large");
+};
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2], cooked[2];
+  uint64_t s_full, p_full, dp_full, ds_full;
+  uint64_t dq_full, dq_empty;
+  uint64_t acc_full, acc_empty;
+  uint64_t drain;
+};
+
+// Work item -> (head, key tile) and its query tiles qt0 .. qt0 + nq - 1.  With
+// the causal mask the items go out longest first (key tile 0 sees every query
+// tile) across all heads; without it, head-major so that the items sharing a
+// head's queries run together.
+struct BItem {
+  int bh, kt, qt0, nq;
+};
+__device__ __forceinline__ BItem bwd_item(const BwdTcParams& p, int w) {
+  BItem it;
+  if (p.causal) {
+    it.kt = w / p.BH;
+    it.bh = w % p.BH;
+    it.qt0 = it.kt;
+    it.nq = p.NT - it.kt;
+  } else {
+    it.bh = w / p.NT;
+    it.kt = w % p.NT;
+    it.qt0 = 0;
+    it.nq = p.NT;
+  }
+  return it;
+}
+
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   gdst),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) {
+  lo = __uint_as_float(v << 16);
+  hi = __uint_as_float(v & 0xffff0000u);
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---------------------------------------------------------------- loader
+template <class Plan, int KD, int MB, int DV>
+__device__ __forceinline__ void bwd_loader(const BwdTcParams& p, const CUtensorMap* vmap,
+                                           const CUtensorMap* domap, uint8_t* smem, BwdBars& bars,
+                                           const WaitCtl& ctl, int items) {
+  prefetch_tmap(vmap);
+  prefetch_tmap(domap);
+  uint32_t g = 0;  // query tiles armed so far
+  int karmed = 0;  // items armed so far
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int w = item_index(k, items);
+    if (w < 0) break;
+    const BItem it = bwd_item(p, w);
+    if (k > 0 && !(ok = wait_or_abort(&bars.kv_empty, (k - 1) & 1, ctl))) break;
+    const size_t ktile = static_cast<size_t>(it.bh) * p.NT + it.kt;
+    mbar_arrive_expect_tx(&bars.kv_full, Plan::kKfBytes + Plan::kBBytes + Plan::kVBytes);
+    bulk_g2s(smem + Plan::kKf, p.Ks + ktile * kTileRows * KD, Plan::kKfBytes, &bars.kv_full);
+    bulk_g2s(smem + Plan::kKb, p.Kb + ktile * kTileRows * MB, Plan::kBBytes, &bars.kv_full);
+#pragma unroll
+    for (int h = 0; h < DV / 64; ++h)
+      tma_load_3d(smem + Plan::kV + h * 16384, vmap, h * 64, it.kt * kTileRows, it.bh,
+                  &bars.kv_full);
+    karmed = k + 1;
+    for (int n = 0; n < it.nq; ++n, ++g) {
+      const int s = g & 1;
+      if (g >= 2 && !(ok = wait_or_abort(&bars.q_empty[s], ((g >> 1) - 1) & 1, ctl))) break;
+      const int qt = it.qt0 + n;
+      const size_t qtile = static_cast<size_t>(it.bh) * p.NT + qt;
+      uint8_t* st = smem + Plan::kRing + s * Plan::kStageBytes;
+      mbar_arrive_expect_tx(&bars.q_full[s],
+                            Plan::kVBytes + Plan::kKfBytes + Plan::kBBytes + Plan::kStatBytes);
+#pragma unroll
+      for (int h = 0; h < DV / 64; ++h)
+        tma_load_3d(st + Plan::kStDo + h * 16384, domap, h * 64, qt * kTileRows, it.bh,
+                    &bars.q_full[s]);
+      bulk_g2s(st + Plan::kStQf, p.Qs + qtile * kTileRows * KD, Plan::kKfBytes, &bars.q_full[s]);
+      bulk_g2s(st + Plan::kStQb, p.Qb + qtile * kTileRows * MB, Plan::kBBytes, &bars.q_full[s]);
+      bulk_g2s(st + Plan::kStStat, p.stats + qtile * 4 * kTileRows, Plan::kStatBytes,
+               &bars.q_full[s]);
+    }
+  }
+  // every copy this thread started lands before the CTA's memory is released
+  if (karmed > 0) mbar_wait(&bars.kv_full, (karmed - 1) & 1, ctl.limit_ns);
+  for (uint32_t s = 0; s < 2; ++s) {
+    const uint32_t n = g > s ? (g - s + 1) / 2 : 0;  // times stage s was armed
+    if (n > 0) mbar_wait(&bars.q_full[s], (n - 1) & 1, ctl.limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------- issuer
+template <class Plan, int KD, int MB, int DV, bool F16OPS>
+__device__ __forceinline__ void bwd_issuer(const BwdTcParams& p, uint32_t sbase, uint32_t tb,
+                                           BwdBars& bars, const WaitCtl& ctl, int items) {
+  constexpr uint32_t kIdS = idesc_f16(128, 128, F16OPS ? kFmtF16 : kFmtBF16, 0, 0);
+  constexpr uint32_t kIdDP = idesc_f16(128, 128, kFmtBF16, 0, 0);
+  constexpr uint32_t kIdDV = idesc_f16(128, DV, kFmtBF16, 0, 1);
+  constexpr uint32_t kIdDK = idesc_f16(128, MB, kFmtBF16, 0, 1);
+  constexpr uint32_t kIdDQ = idesc_f16(128, MB, kFmtBF16, 1, 1);
+  // K-major interleaved score operands; K-major SW128 V / dO (score-like use);
+  // MN-major SW128 dO (value-like use) and dS; MN-major interleaved bf16 Qp / Kp
+  const uint64_t dKf = smem_desc(sbase + Plan::kKf, 2048, 128, kLayoutInterleave);
+  const uint64_t dKb = smem_desc(sbase + Plan::kKb, 128, 2048, kLayoutInterleave);
+  const uint64_t dVk = smem_desc(sbase + Plan::kV, 16, 1024, kLayoutSwizzle128);
+  const uint64_t dDs = smem_desc(sbase + Plan::kDs, 16384, 1024, kLayoutSwizzle128);
+  uint64_t dQf[2], dQb[2], dDoK[2], dDoM[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const uint32_t st = sbase + Plan::kRing + s * Plan::kStageBytes;
+    dQf[s] = smem_desc(st + Plan::kStQf, 2048, 128, kLayoutInterleave);
+    dQb[s] = smem_desc(st + Plan::kStQb, 128, 2048, kLayoutInterleave);
+    dDoK[s] = smem_desc(st + Plan::kStDo, 16, 1024, kLayoutSwizzle128);
+    dDoM[s] = smem_desc(st + Plan::kStDo, 16384, 1024, kLayoutSwizzle128);
+  }
+  auto issue_s = [&](int s) {  // S^T = Kf Qf^T
+    const uint64_t b = s ? dQf[1] : dQf[0];
+#pragma unroll
+    for (int k = 0; k < KD / 16; ++k)
+      mma_ss(tb + Plan::kColS, dKf + (k * 4096 >> 4), b + (k * 4096 >> 4), kIdS, k > 0);
+    mma_commit(&bars.s_full);
+  };
+  auto issue_dp = [&](int s) {  // dP^T = V dO^T, depth d_v
+    const uint64_t b = s ? dDoK[1] : dDoK[0];
+#pragma unroll
+    for (int k = 0; k < DV / 16; ++k) {
+      const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+      mma_ss(tb + Plan::kColDP, dVk + off, b + off, kIdDP, k > 0);
+    }
+    mma_commit(&bars.dp_full);
+  };
+  auto issue_dv = [&](int s, uint32_t acc) {  // dV += P^T dO, depth = 128 queries
+    const uint64_t b = s ? dDoM[1] : dDoM[0];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mma_ts(tb + Plan::kColDV, tb + Plan::kColS + 64 * (k >> 2) + 8 * (k & 3),
+             b + (k * 2048 >> 4), kIdDV, k > 0 ? 1u : acc);
+  };
+  auto issue_dk = [&](int s, uint32_t acc) {  // dKp += dS^T Qb
+    const uint64_t b = s ? dQb[1] : dQb[0];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mma_ts(tb + Plan::kColDK, tb + Plan::kColDP + 64 * (k >> 2) + 8 * (k & 3),
+             b + (k * 256 >> 4), kIdDK, k > 0 ? 1u : acc);
+  };
+  auto issue_dq = [&]() {  // dQp = dS Kb, depth = 128 keys
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mma_ss(tb + Plan::kColDQ, dDs + (k * 2048 >> 4), dKb + (k * 256 >> 4), kIdDQ, k > 0);
+  };
+
+  uint32_t g = 0;  // query tiles issued so far
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int w = item_index(k, items);
+    if (w < 0) break;
+    const BItem it = bwd_item(p, w);
+    if (!(ok = wait_or_abort(&bars.kv_full, k & 1, ctl))) break;
+    for (int n = 0; n < it.nq; ++n, ++g) {
+      const int s = g & 1;
+      if (n == 0) {
+        if (!(ok = wait_or_abort(&bars.q_full[s], (g >> 1) & 1, ctl))) break;
+        tc_fence_after();
+        issue_s(s);
+      }
+      issue_dp(s);
+      if (!(ok = wait_or_abort(&bars.p_full, g & 1, ctl))) break;
+      // the first dV product of an item overwrites the accumulators: the
+      // previous item's dV and dKp must have been read out
+      if (n == 0 && k > 0 && !(ok = wait_or_abort(&bars.acc_empty, (k - 1) & 1, ctl))) break;
+      tc_fence_after();
+      issue_dv(s, n > 0 ? 1u : 0u);
+      if (n + 1 < it.nq) {
+        const int s1 = (g + 1) & 1;
+        if (!(ok = wait_or_abort(&bars.q_full[s1], ((g + 1) >> 1) & 1, ctl))) break;
+        tc_fence_after();
+        issue_s(s1);
+      }
+      if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
+      tc_fence_after();
+      issue_dk(s, n > 0 ? 1u : 0u);
+      mma_commit(&bars.q_empty[s]);  // stage s: last product reading it is issued
+      if (g > 0 && !(ok = wait_or_abort(&bars.dq_empty, (g - 1) & 1, ctl))) break;
+      tc_fence_after();
+      issue_dq();
+      mma_commit(&bars.dq_full);
+    }
+    if (!ok) break;
+    mma_commit(&bars.kv_empty);
+    mma_commit(&bars.acc_full);
+  }
+  mma_commit(&bars.drain);
+  mbar_wait(&bars.drain, 0, ctl.limit_ns);  // own MMAs in flight
+}
+
+// ---------------------------------------------------------------- gradient warpgroups
+template <class Plan>
+__device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem, uint32_t sbase,
+                                             uint32_t tb, BwdBars& bars, const WaitCtl& ctl,
+                                             int items, int warp, int lane) {
+  const int wg = warp >> 2;                 // query columns 64 wg .. 64 wg + 63
+  const int r = (warp & 3) * 32 + lane;     // key row of the tile == TMEM lane
+  const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const uint32_t tS = lane_base + Plan::kColS + 64 * wg;
+  const uint32_t tDP = lane_base + Plan::kColDP + 64 * wg;
+  const uint32_t srow = sbase + Plan::kDs + wg * 16384 + r * 128;  // this row of the dS tile
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
+  const uint64_t alpha2 = pack_f32x2(p.alpha, p.alpha);
+  uint32_t g = 0;
+  for (int k = 0;; ++k) {
+    const int w = item_index(k, items);
+    if (w < 0) break;
+    const BItem it = bwd_item(p, w);
+    const bool row_ok = it.kt * kTileRows + r < p.N;
+    bool ok = true;
+    for (int n = 0; n < it.nq; ++n, ++g) {
+      const int s = g & 1;
+      const int qt = it.qt0 + n;
+      const float* stp = reinterpret_cast<const float*>(smem + Plan::kRing + s * Plan::kStageBytes +
+                                                        Plan::kStStat) + 64 * wg;
+      // ---- P-phase: P^T = exp2(S^T a - L log2 e), masked, bf16 over S^T
+      if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars.s_full, g & 1, ctl) &&
+                                             wait_or_abort(&bars.cooked[s], (g >> 1) & 1, ctl))))
+        break;
+      tc_fence_after();
+      uint32_t x0[32], x1[32];
+      tmem_ld32(tS, x0);
+      tmem_ld32(tS + 32, x1);
+      tmem_wait_ld();
+      // query column c (of this warpgroup's 64) is visible to key row r unless
+      // the causal mask hides it on the diagonal tile; padded key rows see nothing
+      const int cmin = !row_ok ? 64 : ((p.causal && qt == it.kt) ? r - 64 * wg : 0);
+      uint32_t pk[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const int c = 32 * h + 4 * i4;
+          const float4 a4 = *reinterpret_cast<const float4*>(stp + 3 * kTileRows + c);
+          const float4 l4 = *reinterpret_cast<const float4*>(stp + kTileRows + c);
+          const uint32_t* xv = h == 0 ? x0 : x1;
+          float y0, y1, y2, y3;
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(xv[4 * i4]), __uint_as_float(xv[4 * i4 + 1])),
+                                 pack_f32x2(a4.x, a4.y), pack_f32x2(l4.x, l4.y)),
+                       y0, y1);
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(xv[4 * i4 + 2]), __uint_as_float(xv[4 * i4 + 3])),
+                                 pack_f32x2(a4.z, a4.w), pack_f32x2(l4.z, l4.w)),
+                       y2, y3);
+          float e0 = ex2(y0), e1 = ex2(y1), e2 = ex2(y2), e3 = ex2(y3);
+          if (cmin > 0) {
+            e0 = c < cmin ? 0.f : e0;
+            e1 = c + 1 < cmin ? 0.f : e1;
+            e2 = c + 2 < cmin ? 0.f : e2;
+            e3 = c + 3 < cmin ? 0.f : e3;
+          }
+          pk[16 * h + 2 * i4] = pack_bf16x2(e0, e1);
+          pk[16 * h + 2 * i4 + 1] = pack_bf16x2(e2, e3);
+        }
+      }
+      {
+        uint32_t lo[16], hi[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          lo[i] = pk[i];
+          hi[i] = pk[16 + i];
+        }
+        tmem_st16(tS, lo);
+        tmem_st16(tS + 16, hi);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full);
+
+      // ---- dS-phase: dS^T = P^T (dP^T alpha - D alpha), bf16 over dP^T and into the dS tile
+      if (!(ok = __all_sync(0xffffffffu,
+                            wait_or_abort(&bars.dp_full, g & 1, ctl) &&
+                                (g == 0 || wait_or_abort(&bars.dq_full, (g - 1) & 1, ctl)))))
+        break;
+      tc_fence_after();
+      tmem_ld32(tDP, x0);
+      tmem_ld32(tDP + 32, x1);
+      tmem_wait_ld();
+      uint32_t dk[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const int c = 32 * h + 4 * i4;
+          const float4 d4 = *reinterpret_cast<const float4*>(stp + 2 * kTileRows + c);
+          const uint32_t* xv = h == 0 ? x0 : x1;
+          float p0, p1, p2, p3;
+          unpack_bf16x2(pk[16 * h + 2 * i4], p0, p1);
+          unpack_bf16x2(pk[16 * h + 2 * i4 + 1], p2, p3);
+          const uint64_t u01 = fma_f32x2(
+              pack_f32x2(__uint_as_float(xv[4 * i4]), __uint_as_float(xv[4 * i4 + 1])), alpha2,
+              pack_f32x2(d4.x, d4.y));
+          const uint64_t u23 = fma_f32x2(
+              pack_f32x2(__uint_as_float(xv[4 * i4 + 2]), __uint_as_float(xv[4 * i4 + 3])), alpha2,
+              pack_f32x2(d4.z, d4.w));
+          float s0, s1, s2, s3;
+          unpack_f32x2(mul_f32x2(u01, pack_f32x2(p0, p1)), s0, s1);
+          unpack_f32x2(mul_f32x2(u23, pack_f32x2(p2, p3)), s2, s3);
+          dk[16 * h + 2 * i4] = pack_bf16x2(s0, s1);
+          dk[16 * h + 2 * i4 + 1] = pack_bf16x2(s2, s3);
+        }
+      }
+      {
+        uint32_t lo[16], hi[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          lo[i] = dk[i];
+          hi[i] = dk[16 + i];
+        }
+        tmem_st16(tDP, lo);
+        tmem_st16(tDP + 16, hi);
+      }
+      // dS (M = queries) for the dQp product: 16-byte chunk q of this key row
+      // holds queries 64 wg + 8q .. +7 and sits at chunk q ^ (r % 8)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(srow + ((q ^ sw) << 4), dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ds_full);
+    }
+    if (!ok) break;
+  }
+}
+
+// ---------------------------------------------------------------- epilogue warpgroup
+template <class Plan, int MB, int DV>
+__device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem, uint32_t sbase,
+                                             uint32_t tb, BwdBars& bars, const WaitCtl& ctl,
+                                             int items, int warp, int lane) {
+  const int e = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQp), key row (dV, dKp)
+  const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  constexpr int kChunks = MB / 4;  // 16-byte chunks per dQp row
+  // swizzle of the staging tile (and of the dQp accumulator's tiles): chunk q of
+  // row e sits at q ^ (128-byte line of the row % kChunks)
+  const uint32_t dsw = static_cast<uint32_t>((e * MB / 32) & (kChunks - 1));
+  const uint32_t stage_row = sbase + Plan::kDq + e * MB * 4;
+
+  // the column factors a_i = (Q row multiplier) x (K tile multiplier) of tile gg
+  auto cook = [&](uint32_t gg, const BItem& itc) -> bool {
+    const int s = gg & 1;
+    if (!__all_sync(0xffffffffu, wait_or_abort(&bars.q_full[s], (gg >> 1) & 1, ctl))) return false;
+    float* stp = reinterpret_cast<float*>(smem + Plan::kRing + s * Plan::kStageBytes + Plan::kStStat);
+    const float km = __ldg(p.kmul + static_cast<size_t>(itc.bh) * p.NT + itc.kt);
+    stp[3 * kTileRows + e] = stp[e] * km;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.cooked[s]);
+    return true;
+  };
+
+  int w = item_index(0, items);
+  BItem it{};
+  if (w >= 0) it = bwd_item(p, w);
+  bool ok = w < 0 || cook(0, it);
+  uint32_t g = 0;
+  for (int k = 0; w >= 0; ++k) {
+    const int wn = item_index(k + 1, items);
+    BItem itn{};
+    if (wn >= 0) itn = bwd_item(p, wn);
+    for (int n = 0; n < it.nq; ++n, ++g) {
+      // the next tile's column factors first: the gradient warpgroups need them
+      // before this tile's dQp is even computed
+      if (ok && n + 1 < it.nq) ok = cook(g + 1, it);
+      else if (ok && wn >= 0) ok = cook(g + 1, itn);
+      ok = ok && __all_sync(0xffffffffu, wait_or_abort(&bars.dq_full, g & 1, ctl));
+      // the four warps decide together, so that they meet the barriers below as one
+      if (!(ok = named_bar_and(kEpiBar, 128, ok))) break;
+      tc_fence_after();
+      uint32_t v[MB];
+      if constexpr (MB == 32) {
+        tmem_ld32(lane_base + Plan::kColDQ, v);
+      } else {
+        tmem_ld16(lane_base + Plan::kColDQ, v);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dq_empty);
+      if (e == 0) bulk_wait_group_read<0>();  // the previous reduce has read the staging tile
+      named_bar_sync(kEpiBar, 128);
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q)
+        st_shared_v4(stage_row + ((q ^ dsw) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(kEpiBar, 128);
+      if (e == 0) {
+        const size_t qtile = static_cast<size_t>(it.bh) * p.NT + it.qt0 + n;
+        bulk_reduce_add_f32(p.dqacc + qtile * kTileRows * MB, sbase + Plan::kDq, Plan::kDqBytes);
+        bulk_commit_group();
+      }
+    }
+    if (!ok) break;
+    // ---- item end: dKp and dV rows of the key tile
+    ok = __all_sync(0xffffffffu, wait_or_abort(&bars.acc_full, k & 1, ctl));
+    if (!(ok = named_bar_and(kEpiBar, 128, ok))) break;
+    tc_fence_after();
+    const int row = it.kt * kTileRows + e;
+    const bool wr = row < p.N;
+    {
+      uint32_t v[MB];
+      if constexpr (MB == 32) {
+        tmem_ld32(lane_base + Plan::kColDK, v);
+      } else {
+        tmem_ld16(lane_base + Plan::kColDK, v);
+      }
+      tmem_wait_ld();
+      if (wr) {
+        float4* dst = reinterpret_cast<float4*>(p.dkp + (static_cast<size_t>(it.bh) * p.N + row) * MB);
+#pragma unroll
+        for (int q = 0; q < MB / 4; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+    float4* dvrow = reinterpret_cast<float4*>(p.dv_out + (static_cast<size_t>(it.bh) * p.N + row) * DV);
+#pragma unroll
+    for (int c0 = 0; c0 < DV; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(lane_base + Plan::kColDV + c0, v);
+      tmem_wait_ld();
+      if (c0 + 32 == DV) {  // every accumulator column is read: the next item may start
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.acc_empty);
+      }
+      if (wr) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dvrow[c0 / 4 + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+    w = wn;
+    it = itn;
+  }
+  if (e == 0) bulk_wait_group_read<0>();  // the reduce-adds have read shared memory
+}
+
+template <int KD, int MB, int DV, bool F16OPS>
+__global__ void __launch_bounds__(kBThreads, 1)
+    bwd_ws_kernel(const BwdTcParams p, const __grid_constant__ CUtensorMap vmap,
+                  const __grid_constant__ CUtensorMap domap) {
+  using Plan = BwdPlan<KD, MB, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int items = p.BH * p.NT;
+  const WaitCtl ctl{&abort_sh, p.err, p.limit_ns};
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+
+  if (warp == kBMmaWarp) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bars.kv_full, 1);
+    mbar_init(&bars.kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.cooked[s], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 8);   // one arrival per gradient warp
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ds_full, 8);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_empty, 4);
+    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_empty, 4);
+    mbar_init(&bars.drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base_sh;
+  if (warp < 8) {
+    bwd_gradient<Plan>(p, smem, sbase, tb, bars, ctl, items, warp, lane);
+  } else if (warp < 12) {
+    bwd_epilogue<Plan, MB, DV>(p, smem, sbase, tb, bars, ctl, items, warp, lane);
+  } else if (warp == kBLoadWarp) {
+    if (lane == 0) bwd_loader<Plan, KD, MB, DV>(p, &vmap, &domap, smem, bars, ctl, items);
+  } else if (warp == kBMmaWarp) {
+    if (lane == 0) bwd_issuer<Plan, KD, MB, DV, F16OPS>(p, sbase, tb, bars, ctl, items);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBMmaWarp) tmem_dealloc(tb, 512);
+}
+
+int bwd_num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int KD, int MB, int DV, bool F16OPS>
+cudaError_t launch_bwd(const BwdTcParams& p, cudaStream_t stream) {
+  using Plan = BwdPlan<KD, MB, DV>;
+  auto kern = bwd_ws_kernel<KD, MB, DV, F16OPS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan::kLaunch);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(p.BH) * p.NT;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int sms = bwd_num_sms();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+  kern<<<grid, kBThreads, Plan::kLaunch, stream>>>(p, p.vmap, p.domap);
+  return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_bwd_dv(const BwdTcParams& p, cudaStream_t stream) {
+  if (p.m == 16 && !p.f16_ops && p.KD == 48) return launch_bwd<48, 16, DV, false>(p, stream);
+  if (p.m == 32 && p.f16_ops && p.KD == 32) return launch_bwd<32, 32, DV, true>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------- small kernels
+// One warp per padded query row: stats[bh][tile][plane][r].
+__global__ void __launch_bounds__(256)
+    bwd_stats_kernel(const __nv_bfloat16* __restrict__ dO, const float* __restrict__ out,
+                     const float* __restrict__ lse, const float* __restrict__ qmul,
+                     float* __restrict__ stats, int BH, int N, int NT, int dv, float alpha) {
+  const long long R = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long long rows = static_cast<long long>(BH) * NT * kTileRows;
+  if (R >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int bh = static_cast<int>(R / (static_cast<long long>(NT) * kTileRows));
+  const int i = static_cast<int>(R % (static_cast<long long>(NT) * kTileRows));
+  float qm = 0.f, nl = -INFINITY, dn = 0.f;
+  if (i < N) {
+    const size_t off = (static_cast<size_t>(bh) * N + i) * dv;
+    float acc = 0.f;
+    for (int c = lane; c < dv; c += 32) acc = fmaf(__bfloat162float(dO[off + c]), out[off + c], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    qm = qmul[R];
+    nl = -lse[static_cast<size_t>(bh) * N + i] * 1.4426950408889634f;
+    dn = -acc * alpha;
+  }
+  if (lane < 4) {
+    const size_t base = ((static_cast<size_t>(bh) * NT + i / kTileRows) * 4) * kTileRows + i % kTileRows;
+    const float v = lane == 0 ? qm : lane == 1 ? nl : lane == 2 ? dn : 0.f;
+    stats[base + static_cast<size_t>(lane) * kTileRows] = v;
+  }
+}
+
+__device__ __forceinline__ void split_store(float v, uint16_t* hi, uint16_t* lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  *hi = __bfloat16_as_ushort(h);
+  *lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
+}
+
+// element (bh, i, c), i < N, c < m: dQp from its swizzled tile, dKp from its row
+__global__ void bwd_split_kernel(const float* __restrict__ dqacc, const float* __restrict__ dkp,
+                                 uint16_t* __restrict__ xq, uint16_t* __restrict__ xk, int BH,
+                                 int N, int NT, int m) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(BH) * N * m;
+  if (t >= total) return;
+  const int c = static_cast<int>(t % m);
+  const long long row = t / m;  // bh * N + i
+  const int bh = static_cast<int>(row / N), i = static_cast<int>(row % N);
+  const int e = i % kTileRows, chunks = m / 4;
+  const int phys = (c / 4) ^ ((e * m / 32) & (chunks - 1));
+  const size_t src = ((static_cast<size_t>(bh) * NT + i / kTileRows) * kTileRows + e) * m + phys * 4 + c % 4;
+  const size_t dst = static_cast<size_t>(row) * 2 * m + c;
+  split_store(dqacc[src], xq + dst, xq + dst + m);
+  split_store(dkp[static_cast<size_t>(row) * m + c], xk + dst, xk + dst + m);
+}
+
+__global__ void bwd_dup_p_kernel(const __nv_bfloat16* __restrict__ P, uint16_t* __restrict__ P2,
+                                 long long n, int m) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n) return;  // n = H * d * 2m
+  const int c2 = static_cast<int>(t % (2 * m));
+  const long long hl = t / (2 * m);
+  P2[t] = __bfloat16_as_ushort(P[hl * m + c2 % m]);
+}
+
+__global__ void bwd_fold_kernel(const float* __restrict__ R, float* __restrict__ dP, long long n,
+                                int m) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n) return;  // n = H * d * m
+  const int c = static_cast<int>(t % m);
+  const long long hl = t / m;
+  dP[t] = R[hl * 2 * m + c] + R[hl * 2 * m + m + c];
+}
+
+unsigned blocks_for(long long n, int per) { return static_cast<unsigned>((n + per - 1) / per); }
+
+}  // namespace
+
+bool bwd_tc_supported(int m, int dv) { return (m == 16 || m == 32) && (dv == 64 || dv == 128); }
+
+cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream) {
+  if (p.dv == 64) return launch_bwd_dv<64>(p, stream);
+  if (p.dv == 128) return launch_bwd_dv<128>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const float* lse,
+                             const float* qmul, float* stats, int BH, int N, int NT, int dv,
+                             float alpha, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(BH) * NT * kTileRows;
+  if (rows == 0) return cudaSuccess;
+  bwd_stats_kernel<<<blocks_for(rows, 8), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N, NT,
+                                                            dv, alpha);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_split(const float* dqacc, const float* dkp, uint16_t* xq, uint16_t* xk,
+                             int BH, int N, int NT, int m, cudaStream_t stream) {
+  const long long n = static_cast<long long>(BH) * N * m;
+  if (n == 0) return cudaSuccess;
+  bwd_split_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(dqacc, dkp, xq, xk, BH, N, NT, m);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dup_p(const __nv_bfloat16* P, uint16_t* P2, int H, int d, int m,
+                             cudaStream_t stream) {
+  const long long n = static_cast<long long>(H) * d * 2 * m;
+  if (n == 0) return cudaSuccess;
+  bwd_dup_p_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(P, P2, n, m);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_fold(const float* R, float* dP, int H, int d, int m, cudaStream_t stream) {
+  const long long n = static_cast<long long>(H) * d * m;
+  if (n == 0) return cudaSuccess;
+  bwd_fold_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(R, dP, n, m);
+  return cudaGetLastError();
+}
+
+}  // namespace spa

@@ -15,6 +15,7 @@ enum class ProjOut : int {
   F16X1 = 1,     // fp16 UMMA tiles, power-of-two row (Q) / tile (K) exponents
   BF16X3 = 2,    // bf16 hi/lo split UMMA tiles, depth 3m
   F16ROWS = 3,   // fp16 rows [BH][out_rows][m] at row out_pos + n, power-of-two row multipliers
+  BF16X1 = 4,    // plain bf16 UMMA tiles (no scale, no multipliers): the backward's product operands
 };
 
 // Score-GEMM operand tiles: 128 rows x KD columns of 16-bit values in the
@@ -55,6 +56,7 @@ struct AttnTcParams {
   int f16_ops;           // 1: fp16 score operands, 0: bf16
   unsigned long long limit_ns;  // time limit of every wait in the kernel
   int inject_stall;      // failure-detection test only: withhold one barrier arrival
+  float* lse;            // optional [BH][N]: row log-sum-exp of the logits (natural log)
 };
 cudaError_t launch_attn_ws(const AttnTcParams& p, cudaStream_t stream);
 
@@ -65,6 +67,7 @@ struct AttnF32Params {
   float* out;            // [BH][N][dv]
   int BH, N, m, dv, causal;
   float scale;           // 1/sqrt(m)
+  float* lse;            // optional [BH][N]: row log-sum-exp of the logits (natural log)
 };
 cudaError_t launch_attn_f32(const AttnF32Params& p, cudaStream_t stream);
 
@@ -91,6 +94,44 @@ struct BwdParams {
 size_t backward_workspace_bytes(const BwdParams& p);
 int backward_group(int B, int H, int N, size_t budget_bytes);
 int run_backward(const BwdParams& p, void* ws, cudaStream_t stream);  // 0, -1 CUDA, -2 cuBLAS
+
+// Fused backward on tcgen05 (bf16 inputs, m in {16, 32}, d_v in {64, 128}).
+// Tiles are 128 rows; NT = ceil(N / 128).
+struct BwdTcParams {
+  const uint16_t* Qs;    // [BH][NT][128*KD] score-operand tiles, exactly the forward's
+  const uint16_t* Ks;    // [BH][NT][128*KD]
+  const float* kmul;     // [BH][NT] K tile range multipliers
+  const uint16_t* Qb;    // [BH][NT][128*m] bf16 Qp tiles (interleaved layout)
+  const uint16_t* Kb;    // [BH][NT][128*m] bf16 Kp tiles
+  const float* stats;    // [BH][NT][4][128]: Q row multiplier, -lse*log2(e), -D/sqrt(m), 0
+  CUtensorMap vmap;      // V  as 3-D (d_v, N, BH), bf16, 128-byte swizzle, box (64,128,1)
+  CUtensorMap domap;     // dO as 3-D (d_v, N, BH), same encoding
+  float* dqacc;          // [BH][NT][128*m] fp32 dQp accumulator (zeroed; swizzled rows)
+  float* dkp;            // [BH][N][m] fp32 dKp
+  float* dv_out;         // [BH][N][d_v] fp32 dV
+  int* err;
+  int BH, N, NT, KD, m, dv, causal;
+  int f16_ops;           // 1: fp16 score operands, 0: bf16 (split) score operands
+  float alpha;           // 1/sqrt(m)
+  unsigned long long limit_ns;
+};
+bool bwd_tc_supported(int m, int dv);
+cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream);
+// stats for the backward: one warp per padded query row
+cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const float* lse,
+                             const float* qmul, float* stats, int BH, int N, int NT, int dv,
+                             float alpha, cudaStream_t stream);
+// dQp (swizzled tiles) and dKp (rows) -> bf16 hi | lo rows [BH][N][2m]
+cudaError_t launch_bwd_split(const float* dqacc, const float* dkp, uint16_t* xq, uint16_t* xk,
+                             int BH, int N, int NT, int m, cudaStream_t stream);
+// P2[h] = [P_h | P_h] (bf16 [H][d][2m]);  dP[h][l][c] = R[h][l][c] + R[h][l][m + c]
+cudaError_t launch_bwd_dup_p(const __nv_bfloat16* P, uint16_t* P2, int H, int d, int m,
+                             cudaStream_t stream);
+cudaError_t launch_bwd_fold(const float* R, float* dP, int H, int d, int m, cudaStream_t stream);
+// dq, dk, dP from the split dQp / dKp rows (library GEMMs on bf16, fp32 accumulation)
+int run_backward_post(const void* q, const void* k, const uint16_t* P2, const uint16_t* xq,
+                      const uint16_t* xk, float* R, float* dq, float* dk, float* dP, int B,
+                      int H, int N, int d, int m, cudaStream_t stream);
 
 // Single-query attention against the projected key cache, split over key chunks.
 constexpr int kDecodeMaxChunk = 8192;  // keys per chunk (scores in shared memory)

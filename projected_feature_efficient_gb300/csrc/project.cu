@@ -27,6 +27,8 @@
 //   F16ROWS projected key cache rows (decode): fp16, row-major [BH][rows][m],
 //           written at rows pos .. pos+N-1, each row divided by a power of two
 //           chosen from its own max |value| (multiplier kept per row).
+//   BF16X1  plain bf16 tiles of Xp (no scale, no multipliers): the operands of
+//           the backward's dQp = dS Kp and dKp = dS^T Qp products.
 //   BF16X3  score-GEMM operand tiles in bf16, each value split v = hi + lo
 //           (hi = bf16(v), lo = bf16(v - hi)); Q rows are stored [hi|hi|lo] and
 //           K rows [hi|lo|hi], so one GEMM of depth 3m sums
@@ -99,7 +101,10 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, float (&acc)[MP]
   for (int k = 0; k < MP; ++k) acc[k] *= sc;
 
   uint16_t vals[KD];
-  if constexpr (MODE == ProjOut::F16X1) {
+  if constexpr (MODE == ProjOut::BF16X1) {
+#pragma unroll
+    for (int k = 0; k < MP; ++k) vals[k] = bf16_bits(acc[k]);
+  } else if constexpr (MODE == ProjOut::F16X1) {
     float amax = 0.f;
 #pragma unroll
     for (int k = 0; k < MP; ++k) amax = fmaxf(amax, fabsf(acc[k]));
@@ -457,6 +462,17 @@ cudaError_t launch_project(const ProjParams& p, cudaStream_t stream) {
       case 128:
         return tc ? launch_tc_mp<128, ProjOut::F16ROWS>(p, stream)
                   : launch_one<__nv_bfloat16, 128, ProjOut::F16ROWS>(p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.mode == ProjOut::BF16X1) {
+    switch (p.m) {
+      case 16:
+        return tc ? launch_tc_mp<16, ProjOut::BF16X1>(p, stream)
+                  : launch_one<__nv_bfloat16, 16, ProjOut::BF16X1>(p, stream);
+      case 32:
+        return tc ? launch_tc_mp<32, ProjOut::BF16X1>(p, stream)
+                  : launch_one<__nv_bfloat16, 32, ProjOut::BF16X1>(p, stream);
       default: return cudaErrorInvalidValue;
     }
   }

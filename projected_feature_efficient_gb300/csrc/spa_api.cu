@@ -180,7 +180,8 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int causal,
               int dtype, const void* ws, cudaStream_t stream,
-              unsigned long long limit_ns = kWaitLimitNs, int inject_stall = 0) {
+              unsigned long long limit_ns = kWaitLimitNs, int inject_stall = 0,
+              float* lse = nullptr) {
   const Layout L = make_layout(B, H, N, m, dtype);
   const int BH = B * H;
   const char* w = static_cast<const char*>(ws);
@@ -196,6 +197,7 @@ int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int
     ap.dv = dv;
     ap.causal = causal != 0;
     ap.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
+    ap.lse = lse;
     return cuda_status(spa::launch_attn_f32(ap, stream));
   }
   int st;
@@ -220,6 +222,7 @@ int run_apply(const void* v, float* out, int B, int H, int N, int m, int dv, int
   ap.f16_ops = L.mode == ProjOut::F16X1;
   ap.limit_ns = limit_ns;
   ap.inject_stall = inject_stall;
+  ap.lse = lse;
   return cuda_status(spa::launch_attn_ws(ap, stream));
 }
 
@@ -324,6 +327,244 @@ int host_forward(const char* q, const char* k, const char* v, const char* P, flo
   }
   if (ev_begin) cudaEventDestroy(ev_begin);
   return st;
+}
+
+// ---------------------------------------------------------------- fused backward
+// Workspace of the fused backward: the forward's prepared operands (so that
+// the recomputed scores are bit-identical to the forward's), bf16 Qp / Kp
+// tiles for the gradient products, the row statistics, the dQp accumulator,
+// dKp, their bf16 hi | lo rows, [P_h | P_h], the projection-gradient partial
+// R, and (when the caller has no log-sum-exp) lse plus a scratch output.
+struct BwdLayout {
+  Layout fwd;
+  size_t qb = 0, kb = 0, stats = 0, dqacc = 0, dkp = 0, xq = 0, xk = 0, p2 = 0, R = 0;
+  size_t lse = 0, out2 = 0, total = 0;
+};
+
+BwdLayout make_bwd_layout(int B, int H, int N, int d, int m, int dv, bool own_lse) {
+  BwdLayout L;
+  L.fwd = make_layout(B, H, N, m, SPA_BF16);
+  const size_t BH = static_cast<size_t>(B) * H, rows = BH * L.fwd.NT * spa::kTileRows;
+  size_t o = L.fwd.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.qb = take(rows * m * 2);
+  L.kb = take(rows * m * 2);
+  L.stats = take(rows * 4 * sizeof(float));
+  L.dqacc = take(rows * m * sizeof(float));
+  L.dkp = take(BH * N * m * sizeof(float));
+  L.xq = take(BH * N * 2 * m * 2);
+  L.xk = take(BH * N * 2 * m * 2);
+  L.p2 = take(static_cast<size_t>(H) * d * 2 * m * 2);
+  L.R = take(static_cast<size_t>(H) * d * 2 * m * sizeof(float));
+  if (own_lse) {
+    L.lse = take(BH * N * sizeof(float));
+    L.out2 = take(BH * N * dv * sizeof(float));
+  }
+  L.total = o;
+  return L;
+}
+
+bool bwd_fused_eligible(int m, int dv, int dtype) {
+  return dtype == SPA_BF16 && spa::bwd_tc_supported(m, dv);
+}
+
+// Fused backward, stage 1 on a workspace laid out by make_bwd_layout, after
+// run_prepare has put the forward's score operands at its start: the bf16
+// Qp / Kp tiles, the zeroed dQp accumulator and the row statistics.
+int bwd_stage_inputs(const void* q, const void* k, const void* P, const float* out,
+                     const float* lse, const void* dO, int B, int H, int N, int d, int m, int d_v,
+                     char* w, cudaStream_t stream) {
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
+  const int BH = B * H, NT = L.fwd.NT;
+  int st;
+  spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, SPA_BF16, L.fwd, w);
+  pp.mode = ProjOut::BF16X1;
+  pp.out[0] = w + L.qb;
+  pp.out[1] = w + L.kb;
+  pp.mul[0] = pp.mul[1] = nullptr;
+  pp.qscale = 1.f;
+  pp.use_tc = 1;
+  if (spa::project_tc_eligible(pp)) {
+    if ((st = encode_bf16_rows(&pp.xmap[0], q, d, N, BH))) return st;
+    if ((st = encode_bf16_rows(&pp.xmap[1], k, d, N, BH))) return st;
+    if ((st = device_error_ptr(&pp.err))) return st;
+  }
+  if ((st = cuda_status(spa::launch_project(pp, stream)))) return st;
+  const float alpha = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
+  if ((st = cuda_status(cudaMemsetAsync(w + L.dqacc, 0,
+                                        static_cast<size_t>(BH) * NT * spa::kTileRows * m *
+                                            sizeof(float),
+                                        stream))))
+    return st;
+  return cuda_status(spa::launch_bwd_stats(
+      static_cast<const __nv_bfloat16*>(dO), out, lse,
+      reinterpret_cast<const float*>(w + L.fwd.qmul), reinterpret_cast<float*>(w + L.stats), BH, N,
+      NT, d_v, alpha, stream));
+}
+
+// Fused backward, stage 2: the tensor-core kernel (dV, dKp, dQp).
+int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int N, int d, int m,
+                     int d_v, int causal, char* w, cudaStream_t stream) {
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
+  const int BH = B * H;
+  int st;
+  spa::BwdTcParams bp{};
+  if ((st = encode_bf16_rows(&bp.vmap, v, d_v, N, BH))) return st;
+  if ((st = encode_bf16_rows(&bp.domap, dO, d_v, N, BH))) return st;
+  if ((st = device_error_ptr(&bp.err))) return st;
+  bp.Qs = reinterpret_cast<const uint16_t*>(w + L.fwd.qs);
+  bp.Ks = reinterpret_cast<const uint16_t*>(w + L.fwd.ks);
+  bp.kmul = reinterpret_cast<const float*>(w + L.fwd.kmul);
+  bp.Qb = reinterpret_cast<const uint16_t*>(w + L.qb);
+  bp.Kb = reinterpret_cast<const uint16_t*>(w + L.kb);
+  bp.stats = reinterpret_cast<const float*>(w + L.stats);
+  bp.dqacc = reinterpret_cast<float*>(w + L.dqacc);
+  bp.dkp = reinterpret_cast<float*>(w + L.dkp);
+  bp.dv_out = dv;
+  bp.BH = BH;
+  bp.N = N;
+  bp.NT = L.fwd.NT;
+  bp.KD = L.fwd.KD;
+  bp.m = m;
+  bp.dv = d_v;
+  bp.causal = causal != 0;
+  bp.f16_ops = L.fwd.mode == ProjOut::F16X1;
+  bp.alpha = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
+  bp.limit_ns = kWaitLimitNs;
+  return cuda_status(spa::launch_bwd_tc(bp, stream));
+}
+
+// Fused backward, stage 3: dq, dk and dP from dQp and dKp.
+int bwd_stage_finish(const void* q, const void* k, const void* P, float* dq, float* dk, float* dP,
+                     int B, int H, int N, int d, int m, int d_v, char* w, cudaStream_t stream) {
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
+  const int BH = B * H;
+  int st;
+  uint16_t* xq = reinterpret_cast<uint16_t*>(w + L.xq);
+  uint16_t* xk = reinterpret_cast<uint16_t*>(w + L.xk);
+  uint16_t* p2 = reinterpret_cast<uint16_t*>(w + L.p2);
+  if ((st = cuda_status(spa::launch_bwd_split(reinterpret_cast<const float*>(w + L.dqacc),
+                                              reinterpret_cast<const float*>(w + L.dkp), xq, xk,
+                                              BH, N, L.fwd.NT, m, stream))))
+    return st;
+  if ((st = cuda_status(
+           spa::launch_bwd_dup_p(static_cast<const __nv_bfloat16*>(P), p2, H, d, m, stream))))
+    return st;
+  const int rc = spa::run_backward_post(q, k, p2, xq, xk, reinterpret_cast<float*>(w + L.R), dq, dk,
+                                        dP, B, H, N, d, m, stream);
+  return rc ? SPA_ERR_CUDA : SPA_OK;
+}
+
+// The whole fused backward.  lse == NULL: the forward runs once more to
+// produce it (into the layout's own lse and scratch output).
+int run_backward_fused(const void* q, const void* k, const void* v, const void* P, const float* out,
+                       const float* lse, const void* dO, float* dq, float* dk, float* dv,
+                       float* dP, int B, int H, int N, int d, int m, int d_v, int causal, char* w,
+                       cudaStream_t stream) {
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, lse == nullptr);
+  int st = run_prepare(q, k, P, B, H, N, d, m, SPA_BF16, w, stream);
+  if (st) return st;
+  if (lse == nullptr) {
+    float* own = reinterpret_cast<float*>(w + L.lse);
+    st = run_apply(v, reinterpret_cast<float*>(w + L.out2), B, H, N, m, d_v, causal, SPA_BF16, w,
+                   stream, kWaitLimitNs, 0, own);
+    if (st) return st;
+    lse = own;
+  }
+  if ((st = bwd_stage_inputs(q, k, P, out, lse, dO, B, H, N, d, m, d_v, w, stream))) return st;
+  if ((st = bwd_stage_kernel(v, dO, dv, B, H, N, d, m, d_v, causal, w, stream))) return st;
+  return bwd_stage_finish(q, k, P, dq, dk, dP, B, H, N, d, m, d_v, w, stream);
+}
+
+// Checks shared by the staged entry points (fused shapes only).
+int check_bwd_staged(int B, int H, int N, int d, int m, int d_v, int dtype, const void* ws,
+                     size_t ws_bytes) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st) return st;
+  if (d > 128 || !bwd_fused_eligible(m, d_v, dtype)) return SPA_ERR_UNSUPPORTED;
+  if (!ws) return SPA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return SPA_ERR_ALIGN;
+  if (ws_bytes < make_bwd_layout(B, H, N, d, m, d_v, false).total) return SPA_ERR_NOMEM;
+  return SPA_OK;
+}
+
+// The materialised backward (fp32 inputs and the shapes the fused one does not cover).
+int run_backward_general(const void* q, const void* k, const void* v, const void* P,
+                         const float* out, const void* dO, float* dq, float* dk, float* dv,
+                         float* dP, int B, int H, int N, int d, int m, int d_v, int causal,
+                         int dtype, cudaStream_t s) {
+  spa::BwdParams bp{};
+  bp.q = q;
+  bp.k = k;
+  bp.v = v;
+  bp.P = P;
+  bp.dO = dO;
+  bp.out = out;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv_out = dv;
+  bp.dP = dP;
+  bp.B = B;
+  bp.H = H;
+  bp.N = N;
+  bp.d = d;
+  bp.m = m;
+  bp.dv = d_v;
+  bp.causal = causal != 0;
+  bp.bf16 = dtype == SPA_BF16;
+  // N x N blocks of as many heads as fit in 8 GB (at least one head)
+  bp.group = spa::backward_group(B, H, N, size_t(8) << 30);
+  const size_t bytes = spa::backward_workspace_bytes(bp);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  const int rc = spa::run_backward(bp, ws, s);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (rc) return SPA_ERR_CUDA;
+  return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
+}
+
+// Shared by both backward entry points; lse may be NULL.
+int backward_entry(const void* q, const void* k, const void* v, const void* P, const float* out,
+                   const float* lse, const void* dO, float* dq, float* dk, float* dv, float* dP,
+                   int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
+                   void* stream) {
+  int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) {
+    if (!dP) return SPA_ERR_NULL;  // the projection gradient is still defined: zero
+    if (H > 0 && d > 0 && m > 0 &&
+        cudaMemsetAsync(dP, 0, static_cast<size_t>(H) * d * m * sizeof(float),
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SPA_ERR_CUDA;
+    return SPA_OK;
+  }
+  if (st) return st;
+  if (d > 128) return SPA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !P || !out || !dO || !dq || !dk || !dv || !dP) return SPA_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!bwd_fused_eligible(m, d_v, dtype))
+    return run_backward_general(q, k, v, P, out, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal,
+                                dtype, s);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(P) || !aligned16(dO) ||
+      !aligned16(out) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dP))
+    return SPA_ERR_ALIGN;
+  const size_t bytes = make_bwd_layout(B, H, N, d, m, d_v, lse == nullptr).total;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = run_backward_fused(q, k, v, P, out, lse, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal,
+                          static_cast<char*>(ws), s);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st) return st;
+  return cuda_status(fe);
 }
 
 }  // namespace
@@ -603,9 +844,92 @@ int spa_attention_bwd(const void* q, const void* k, const void* v, const void* P
                       const float* out, const void* dO, float* dq, float* dk, float* dv,
                       float* dP, int B, int H, int N, int d, int m, int d_v, int causal, int dtype,
                       void* stream) {
+  return backward_entry(q, k, v, P, out, nullptr, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal,
+                        dtype, stream);
+}
+
+int spa_attention_bwd_lse(const void* q, const void* k, const void* v, const void* P,
+                          const float* out, const float* lse, const void* dO, float* dq, float* dk,
+                          float* dv, float* dP, int B, int H, int N, int d, int m, int d_v,
+                          int causal, int dtype, void* stream) {
+  const int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st != kEmpty && st) return st;
+  if (st != kEmpty && !lse) return SPA_ERR_NULL;
+  return backward_entry(q, k, v, P, out, lse, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal, dtype,
+                        stream);
+}
+
+int spa_attention_fwd_lse(const void* q, const void* k, const void* v, const void* P, float* out,
+                          float* lse, int B, int H, int N, int d, int m, int d_v, int causal,
+                          int dtype, void* stream) {
   int st = check_shape(B, H, N, d, m, d_v, dtype);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if ((st = check_forward_ptrs(q, k, v, P, out))) return st;
+  if (!lse) return SPA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return SPA_ERR_ALIGN;
+  const size_t bytes = make_layout(B, H, N, m, dtype).total;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = run_prepare(q, k, P, B, H, N, d, m, dtype, ws, s);
+  if (!st) st = run_apply(v, out, B, H, N, m, d_v, causal, dtype, ws, s, kWaitLimitNs, 0, lse);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st) return st;
+  return cuda_status(fe);
+}
+
+int spa_attention_bwd_workspace_size(int B, int H, int N, int d, int m, int d_v, int dtype,
+                                     size_t* bytes) {
+  if (!bytes) return SPA_ERR_NULL;
+  const int st = check_shape(B, H, N, d, m, d_v, dtype);
   if (st == kEmpty) {
-    if (!dP) return SPA_ERR_NULL;  // the projection gradient is still defined: zero
+    *bytes = 0;
+    return SPA_OK;
+  }
+  if (st) return st;
+  if (d > 128 || !bwd_fused_eligible(m, d_v, dtype)) return SPA_ERR_UNSUPPORTED;
+  *bytes = make_bwd_layout(B, H, N, d, m, d_v, false).total;
+  return SPA_OK;
+}
+
+int spa_attention_bwd_prepare(const void* q, const void* k, const void* P, const float* out,
+                              const float* lse, const void* dO, int B, int H, int N, int d, int m,
+                              int d_v, int dtype, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  int st = check_bwd_staged(B, H, N, d, m, d_v, dtype, workspace, workspace_bytes);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if (!q || !k || !P || !out || !lse || !dO) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(P) || !aligned16(out) || !aligned16(dO))
+    return SPA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(workspace);
+  if ((st = run_prepare(q, k, P, B, H, N, d, m, SPA_BF16, w, s))) return st;
+  return bwd_stage_inputs(q, k, P, out, lse, dO, B, H, N, d, m, d_v, w, s);
+}
+
+int spa_attention_bwd_apply(const void* v, const void* dO, float* dv, int B, int H, int N, int d,
+                            int m, int d_v, int causal, int dtype, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  int st = check_bwd_staged(B, H, N, d, m, d_v, dtype, workspace, workspace_bytes);
+  if (st == kEmpty) return SPA_OK;
+  if (st) return st;
+  if (!v || !dO || !dv) return SPA_ERR_NULL;
+  if (!aligned16(v) || !aligned16(dO) || !aligned16(dv)) return SPA_ERR_ALIGN;
+  return bwd_stage_kernel(v, dO, dv, B, H, N, d, m, d_v, causal, static_cast<char*>(workspace),
+                          static_cast<cudaStream_t>(stream));
+}
+
+int spa_attention_bwd_finish(const void* q, const void* k, const void* P, float* dq, float* dk,
+                             float* dP, int B, int H, int N, int d, int m, int d_v, int dtype,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_bwd_staged(B, H, N, d, m, d_v, dtype, workspace, workspace_bytes);
+  if (st == kEmpty) {
+    if (!dP) return SPA_ERR_NULL;
     if (H > 0 && d > 0 && m > 0 &&
         cudaMemsetAsync(dP, 0, static_cast<size_t>(H) * d * m * sizeof(float),
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -613,41 +937,12 @@ int spa_attention_bwd(const void* q, const void* k, const void* v, const void* P
     return SPA_OK;
   }
   if (st) return st;
-  if (d > 128) return SPA_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !P || !out || !dO || !dq || !dk || !dv || !dP) return SPA_ERR_NULL;
-  spa::BwdParams bp{};
-  bp.q = q;
-  bp.k = k;
-  bp.v = v;
-  bp.P = P;
-  bp.dO = dO;
-  bp.out = out;
-  bp.dq = dq;
-  bp.dk = dk;
-  bp.dv_out = dv;
-  bp.dP = dP;
-  bp.B = B;
-  bp.H = H;
-  bp.N = N;
-  bp.d = d;
-  bp.m = m;
-  bp.dv = d_v;
-  bp.causal = causal != 0;
-  bp.bf16 = dtype == SPA_BF16;
-  // N x N blocks of as many heads as fit in 8 GB (at least one head)
-  bp.group = spa::backward_group(B, H, N, size_t(8) << 30);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t bytes = spa::backward_workspace_bytes(bp);
-  void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
-  }
-  const int rc = spa::run_backward(bp, ws, s);
-  const cudaError_t fe = cudaFreeAsync(ws, s);
-  if (rc == -2) return SPA_ERR_CUDA;
-  if (rc) return SPA_ERR_CUDA;
-  return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
+  if (!q || !k || !P || !dq || !dk || !dP) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(P) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dP))
+    return SPA_ERR_ALIGN;
+  return bwd_stage_finish(q, k, P, dq, dk, dP, B, H, N, d, m, d_v, static_cast<char*>(workspace),
+                          static_cast<cudaStream_t>(stream));
 }
 
 int spa_selftest_wait_timeout(int limit_ms) {

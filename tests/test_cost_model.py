@@ -83,4 +83,7 @@ def test_backward_flop_and_byte_models():
     # per head and N^2 term: S (2m), dA (2 d_v), dQp (2m), dKp (2m), dV (2 d_v)
     assert bench.bwd_flops(1, 1, 10, 4, 3, 5, False) == 2 * 100 * (9 + 10) + 12 * 10 * 4 * 3
     assert bench.bwd_flops(1, 1, 10, 4, 3, 5, True) == 100 * (9 + 10) + 12 * 10 * 4 * 3
-    assert bench.bwd_bytes(2, 16, 8192) == 10 * 4 * 32 * 8192 * 8192
+    # one fused kernel launch: the five N^2 products only (projections outside)
+    assert bench.bwd_kernel_flops(1, 1, 10, 3, 5, False) == 2 * 100 * (9 + 10)
+    assert bench.bwd_kernel_flops(2, 16, 8192, 32, 128, True) == \
+        2 * 32 * 8192 * 8192 * (96 + 256) / 2
