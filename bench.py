@@ -98,7 +98,8 @@ def load_peaks():
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in ("projected_feature_efficient_gb300/csrc/attn_ws.cu",
-                "projected_feature_efficient_gb300/csrc/ptx.cuh"):
+                "projected_feature_efficient_gb300/csrc/ptx.cuh",
+                "projected_feature_efficient_gb300/csrc/waits.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -595,6 +596,8 @@ def run_backward(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = si.WORKLOADS["C3"]
+    if args.heads:
+        w = w.scaled(H=args.heads)
     B, H, N, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
     q_h, k_h, v_h = si.make_qkv(w, seed=None if rank == 0 else 1000 + w.number + 7919 * rank)
     P_h = si.make_P(w)
@@ -716,7 +719,8 @@ def main(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=None,
-                    help="run C4 with fewer heads (smaller case for profiler captures)")
+                    help="run C4 (or the C3 backward) with fewer heads (smaller case for "
+                         "profiler captures)")
     ap.add_argument("--m", type=int, default=32, choices=(16, 32, 64),
                     help="projection width of the C4 sweep")
     ap.add_argument("--decode", action="store_true",

@@ -144,7 +144,10 @@ SPA_API int spa_attention_apply(const void *v, float *out, int B, int H, int N, 
  * streams forked from and joined back into `stream`: chunk c+1 is copied in
  * and chunk c-1 copied out while chunk c computes.  The result is bit for bit
  * that of spa_attention_fwd.  Device buffers and workspace for three chunks
- * are taken with cudaMallocAsync on `stream` and released before return.
+ * are taken on `stream` from a memory pool the library keeps per device and
+ * released to it before return; the pool holds on to what it has reserved, so
+ * that later calls do not reserve device memory again (spa_host_pool_trim
+ * hands it back to the driver).
  * Page-locked host buffers give asynchronous, full-bandwidth copies; pageable
  * ones work but copy synchronously.  Same shapes and dtypes as
  * spa_attention_fwd.
@@ -152,6 +155,11 @@ SPA_API int spa_attention_apply(const void *v, float *out, int B, int H, int N, 
 SPA_API int spa_attention_fwd_host(const void *q, const void *k, const void *v, const void *P,
                                    float *out, int B, int H, int N, int d, int m, int d_v,
                                    int causal, int dtype, void *stream);
+
+/* spa_host_pool_trim -- releases the current device's unused staging memory
+ * kept by spa_attention_fwd_host (call when no host-buffer forward is running
+ * on that device). */
+SPA_API int spa_host_pool_trim(void);
 
 /*
  * spa_attention_fwd_noalloc -- spa_attention_fwd without any device

@@ -48,6 +48,8 @@ lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
 lib.spa_attention_bwd.argtypes = [_vp] * 10 + [_i] * 8 + [_vp]
 lib.spa_attention_bwd.restype = _i
+lib.spa_host_pool_trim.argtypes = []
+lib.spa_host_pool_trim.restype = _i
 lib.spa_attention_bwd_lse.argtypes = [_vp] * 11 + [_i] * 8 + [_vp]
 lib.spa_attention_bwd_lse.restype = _i
 lib.spa_attention_fwd_lse.argtypes = [_vp] * 6 + [_i] * 8 + [_vp]

@@ -253,6 +253,39 @@ namespace {
 // [h0, h0+n) of batch entry b is the problem (B=1, H=n) on the matching slices
 // of q, k, v, out and P.
 constexpr int kHostSlots = 3;
+
+// The host-buffer forward's device staging comes from a pool of the library's
+// own, one per device, which keeps what it has reserved between calls (the
+// default pool hands memory back to the driver at every synchronisation, and
+// reserving a few GB again costs more than the copies it stages).
+cudaMemPool_t g_host_pool[kMaxDevices] = {};
+std::mutex g_host_pool_mu;
+
+int host_pool(cudaMemPool_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_host_pool_mu);
+  if (!g_host_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return SPA_ERR_CUDA;
+    }
+    uint64_t keep = UINT64_MAX;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaGetLastError();
+      cudaMemPoolDestroy(pool);
+      return SPA_ERR_CUDA;
+    }
+    g_host_pool[dev] = pool;
+  }
+  *out = g_host_pool[dev];
+  return SPA_OK;
+}
 constexpr size_t kHostChunkBytes = size_t(32) << 20;  // aim for at least this per chunk
 constexpr int kHostMaxChunks = 16;
 
@@ -282,8 +315,10 @@ int host_forward(const char* q, const char* k, const char* v, const char* P, flo
     if (e != cudaSuccess && st == SPA_OK) st = SPA_ERR_CUDA;
     return e != cudaSuccess;
   };
-  if (cudaMallocAsync(reinterpret_cast<void**>(&dbuf), kHostSlots * slot_bytes, stream) !=
-      cudaSuccess) {
+  cudaMemPool_t pool = nullptr;
+  if (host_pool(&pool) != SPA_OK) return SPA_ERR_CUDA;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dbuf), kHostSlots * slot_bytes, pool,
+                              stream) != cudaSuccess) {
     cudaGetLastError();
     return SPA_ERR_NOMEM;
   }
@@ -943,6 +978,14 @@ int spa_attention_bwd_finish(const void* q, const void* k, const void* P, float*
     return SPA_ERR_ALIGN;
   return bwd_stage_finish(q, k, P, dq, dk, dP, B, H, N, d, m, d_v, static_cast<char*>(workspace),
                           static_cast<cudaStream_t>(stream));
+}
+
+int spa_host_pool_trim(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_host_pool_mu);
+  if (g_host_pool[dev] && cudaMemPoolTrimTo(g_host_pool[dev], 0) != cudaSuccess) return SPA_ERR_CUDA;
+  return SPA_OK;
 }
 
 int spa_selftest_wait_timeout(int limit_ms) {
