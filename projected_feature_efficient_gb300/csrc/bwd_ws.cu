@@ -26,7 +26,8 @@
 //                            MN-major layout the dQp product reads (dS, M = queries).
 //   warps 8-11   epilogue: per query tile the column factors a_i, then the
 //                dQp tile out of TMEM, through a staging tile, into the
-//                reduce-add; per item the dV and dKp rows.
+//                reduce-add; per item the dV rows (fp32) and the dKp rows
+//                (bf16 hi | lo pairs, what the projection-gradient GEMMs read).
 //   warp 12      loads (one thread): per item the key tile's score operand,
 //                its bf16 Kp tile and V; per query tile a two-slot ring of
 //                dO, the score operand, the bf16 Qp tile and the row statistics.
@@ -132,6 +133,15 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, 
                    gdst),
                "r"(ssrc), "r"(bytes)
                : "memory");
+}
+
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): two values at a time as
+// bf16 pairs (16 significant bits of each value)
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+  hi = static_cast<uint32_t>(__bfloat16_as_ushort(ha)) |
+       (static_cast<uint32_t>(__bfloat16_as_ushort(hb)) << 16);
+  lo = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
 }
 
 __device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) {
@@ -516,12 +526,18 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
         tmem_ld16(lane_base + Plan::kColDK, v);
       }
       tmem_wait_ld();
-      if (wr) {
-        float4* dst = reinterpret_cast<float4*>(p.dkp + (static_cast<size_t>(it.bh) * p.N + row) * MB);
+      if (wr) {  // dKp as bf16 pairs: [hi (m values) | lo (m values)]
+        uint4* dst = reinterpret_cast<uint4*>(p.xk + (static_cast<size_t>(it.bh) * p.N + row) * 2 * MB);
 #pragma unroll
-        for (int q = 0; q < MB / 4; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        for (int q = 0; q < MB / 8; ++q) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            split_pair(__uint_as_float(v[8 * q + 2 * i]), __uint_as_float(v[8 * q + 2 * i + 1]),
+                       hi[i], lo[i]);
+          dst[q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          dst[MB / 8 + q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
       }
     }
     float4* dvrow = reinterpret_cast<float4*>(p.dv_out + (static_cast<size_t>(it.bh) * p.N + row) * DV);
@@ -637,11 +653,14 @@ cudaError_t launch_bwd_dv(const BwdTcParams& p, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------- small kernels
-// One warp per padded query row: stats[bh][tile][plane][r].
+// One warp per padded query row: stats[bh][tile][plane][r].  Lane l reads
+// d_v / 32 consecutive values of dO (bf16) and out (fp32) in one vector load each.
+template <int DV>
 __global__ void __launch_bounds__(256)
     bwd_stats_kernel(const __nv_bfloat16* __restrict__ dO, const float* __restrict__ out,
                      const float* __restrict__ lse, const float* __restrict__ qmul,
-                     float* __restrict__ stats, int BH, int N, int NT, int dv, float alpha) {
+                     float* __restrict__ stats, int BH, int N, int NT, float alpha) {
+  constexpr int E = DV / 32;  // 2 or 4
   const long long R = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const long long rows = static_cast<long long>(BH) * NT * kTileRows;
   if (R >= rows) return;
@@ -650,9 +669,20 @@ __global__ void __launch_bounds__(256)
   const int i = static_cast<int>(R % (static_cast<long long>(NT) * kTileRows));
   float qm = 0.f, nl = -INFINITY, dn = 0.f;
   if (i < N) {
-    const size_t off = (static_cast<size_t>(bh) * N + i) * dv;
+    const size_t off = (static_cast<size_t>(bh) * N + i) * DV + lane * E;
     float acc = 0.f;
-    for (int c = lane; c < dv; c += 32) acc = fmaf(__bfloat162float(dO[off + c]), out[off + c], acc);
+    if constexpr (E == 4) {
+      const uint2 g = __ldg(reinterpret_cast<const uint2*>(dO + off));
+      const float4 o = __ldg(reinterpret_cast<const float4*>(out + off));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+      acc = fmaf(a.x, o.x, fmaf(a.y, o.y, fmaf(b.x, o.z, b.y * o.w)));
+    } else {
+      const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(dO + off));
+      const float2 o = __ldg(reinterpret_cast<const float2*>(out + off));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
+      acc = fmaf(a.x, o.x, a.y * o.y);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     qm = qmul[R];
@@ -666,28 +696,26 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-__device__ __forceinline__ void split_store(float v, uint16_t* hi, uint16_t* lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  *hi = __bfloat16_as_ushort(h);
-  *lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
-}
-
-// element (bh, i, c), i < N, c < m: dQp from its swizzled tile, dKp from its row
-__global__ void bwd_split_kernel(const float* __restrict__ dqacc, const float* __restrict__ dkp,
-                                 uint16_t* __restrict__ xq, uint16_t* __restrict__ xk, int BH,
+// (bh, i, 4-column group) of dQp, i < N: its swizzled tile chunk -> bf16 hi | lo row
+__global__ void bwd_split_kernel(const float* __restrict__ dqacc, uint16_t* __restrict__ xq, int BH,
                                  int N, int NT, int m) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(BH) * N * m;
+  const int chunks = m / 4;
+  const long long total = static_cast<long long>(BH) * N * chunks;
   if (t >= total) return;
-  const int c = static_cast<int>(t % m);
-  const long long row = t / m;  // bh * N + i
+  const int q = static_cast<int>(t % chunks);
+  const long long row = t / chunks;  // bh * N + i
   const int bh = static_cast<int>(row / N), i = static_cast<int>(row % N);
-  const int e = i % kTileRows, chunks = m / 4;
-  const int phys = (c / 4) ^ ((e * m / 32) & (chunks - 1));
-  const size_t src = ((static_cast<size_t>(bh) * NT + i / kTileRows) * kTileRows + e) * m + phys * 4 + c % 4;
-  const size_t dst = static_cast<size_t>(row) * 2 * m + c;
-  split_store(dqacc[src], xq + dst, xq + dst + m);
-  split_store(dkp[static_cast<size_t>(row) * m + c], xk + dst, xk + dst + m);
+  const int e = i % kTileRows;
+  const int phys = q ^ ((e * m / 32) & (chunks - 1));
+  const float4 v = __ldg(reinterpret_cast<const float4*>(
+      dqacc + ((static_cast<size_t>(bh) * NT + i / kTileRows) * kTileRows + e) * m + phys * 4));
+  uint32_t hi0, lo0, hi1, lo1;
+  split_pair(v.x, v.y, hi0, lo0);
+  split_pair(v.z, v.w, hi1, lo1);
+  uint16_t* dst = xq + static_cast<size_t>(row) * 2 * m + 4 * q;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(hi0, hi1);
+  *reinterpret_cast<uint2*>(dst + m) = make_uint2(lo0, lo1);
 }
 
 __global__ void bwd_dup_p_kernel(const __nv_bfloat16* __restrict__ P, uint16_t* __restrict__ P2,
@@ -725,16 +753,22 @@ cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const fl
                              float alpha, cudaStream_t stream) {
   const long long rows = static_cast<long long>(BH) * NT * kTileRows;
   if (rows == 0) return cudaSuccess;
-  bwd_stats_kernel<<<blocks_for(rows, 8), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N, NT,
-                                                            dv, alpha);
+  if (dv == 128)
+    bwd_stats_kernel<128><<<blocks_for(rows, 8), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
+                                                                   NT, alpha);
+  else if (dv == 64)
+    bwd_stats_kernel<64><<<blocks_for(rows, 8), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
+                                                                  NT, alpha);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_split(const float* dqacc, const float* dkp, uint16_t* xq, uint16_t* xk,
-                             int BH, int N, int NT, int m, cudaStream_t stream) {
-  const long long n = static_cast<long long>(BH) * N * m;
+cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, int NT, int m,
+                             cudaStream_t stream) {
+  const long long n = static_cast<long long>(BH) * N * (m / 4);
   if (n == 0) return cudaSuccess;
-  bwd_split_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(dqacc, dkp, xq, xk, BH, N, NT, m);
+  bwd_split_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(dqacc, xq, BH, N, NT, m);
   return cudaGetLastError();
 }
 

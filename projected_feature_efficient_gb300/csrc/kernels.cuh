@@ -15,7 +15,6 @@ enum class ProjOut : int {
   F16X1 = 1,     // fp16 UMMA tiles, power-of-two row (Q) / tile (K) exponents
   BF16X3 = 2,    // bf16 hi/lo split UMMA tiles, depth 3m
   F16ROWS = 3,   // fp16 rows [BH][out_rows][m] at row out_pos + n, power-of-two row multipliers
-  BF16X1 = 4,    // plain bf16 UMMA tiles (no scale, no multipliers): the backward's product operands
 };
 
 // Score-GEMM operand tiles: 128 rows x KD columns of 16-bit values in the
@@ -39,6 +38,7 @@ struct ProjParams {
   CUtensorMap xmap[2];   // x[0], x[1] as 3-D (d, N, BH), bf16, 128-byte swizzle, box (64,128,1)
   int* err;              // device error word
   int out_rows, out_pos; // F16ROWS: rows per (batch, head) of the output, first row written
+  void* out_b16[2];      // tile modes, optional: plain bf16 tiles of Xp, [BH][NT][128*m] u16
 };
 bool project_tc_eligible(const ProjParams& p);
 cudaError_t launch_project(const ProjParams& p, cudaStream_t stream);
@@ -107,7 +107,7 @@ struct BwdTcParams {
   CUtensorMap vmap;      // V  as 3-D (d_v, N, BH), bf16, 128-byte swizzle, box (64,128,1)
   CUtensorMap domap;     // dO as 3-D (d_v, N, BH), same encoding
   float* dqacc;          // [BH][NT][128*m] fp32 dQp accumulator (zeroed; swizzled rows)
-  float* dkp;            // [BH][N][m] fp32 dKp
+  uint16_t* xk;          // [BH][N][2m] dKp rows as bf16 hi | lo
   float* dv_out;         // [BH][N][d_v] fp32 dV
   int* err;
   int BH, N, NT, KD, m, dv, causal;
@@ -121,9 +121,9 @@ cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const float* lse,
                              const float* qmul, float* stats, int BH, int N, int NT, int dv,
                              float alpha, cudaStream_t stream);
-// dQp (swizzled tiles) and dKp (rows) -> bf16 hi | lo rows [BH][N][2m]
-cudaError_t launch_bwd_split(const float* dqacc, const float* dkp, uint16_t* xq, uint16_t* xk,
-                             int BH, int N, int NT, int m, cudaStream_t stream);
+// dQp (swizzled tiles) -> bf16 hi | lo rows [BH][N][2m]
+cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, int NT, int m,
+                             cudaStream_t stream);
 // P2[h] = [P_h | P_h] (bf16 [H][d][2m]);  dP[h][l][c] = R[h][l][c] + R[h][l][m + c]
 cudaError_t launch_bwd_dup_p(const __nv_bfloat16* P, uint16_t* P2, int H, int d, int m,
                              cudaStream_t stream);

@@ -15,6 +15,10 @@
 // Either way every product of two inputs is exact in fp32 and the sums are
 // fp32.  The projection is HBM-bound (about 25 FLOP per byte at d=128, m=32).
 //
+// Tile modes can also write plain bf16 tiles of Xp (no scale, no multipliers;
+// out_b16[which] non-null) in the same pass: the operands of the backward's
+// dQp = dS Kp and dKp = dS^T Qp products.
+//
 // Output modes:
 //   F32     plain fp32 rows, [BH][N][m]  (spa_project, and the fp32 path).
 //   F16X1   score-GEMM operand tiles in fp16.  To keep any input range inside
@@ -27,8 +31,6 @@
 //   F16ROWS projected key cache rows (decode): fp16, row-major [BH][rows][m],
 //           written at rows pos .. pos+N-1, each row divided by a power of two
 //           chosen from its own max |value| (multiplier kept per row).
-//   BF16X1  plain bf16 tiles of Xp (no scale, no multipliers): the operands of
-//           the backward's dQp = dS Kp and dKp = dS^T Qp products.
 //   BF16X3  score-GEMM operand tiles in bf16, each value split v = hi + lo
 //           (hi = bf16(v), lo = bf16(v - hi)); Q rows are stored [hi|hi|lo] and
 //           K rows [hi|lo|hi], so one GEMM of depth 3m sums
@@ -96,15 +98,25 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, float (&acc)[MP]
   }
   uint16_t* tout = static_cast<uint16_t*>(which == 0 ? p.out[0] : p.out[1]) +
                    (static_cast<size_t>(bh) * p.NT + tile) * (kTileRows * KD);
+  if (p.out_b16[which] != nullptr) {  // plain bf16 tile of Xp, same interleaved layout
+    uint16_t* bout = static_cast<uint16_t*>(p.out_b16[which]) +
+                     (static_cast<size_t>(bh) * p.NT + tile) * (kTileRows * MP);
+#pragma unroll
+    for (int c8 = 0; c8 < MP / 8; ++c8) {
+      uint4 w;
+      w.x = bf16_bits(acc[c8 * 8 + 0]) | (static_cast<uint32_t>(bf16_bits(acc[c8 * 8 + 1])) << 16);
+      w.y = bf16_bits(acc[c8 * 8 + 2]) | (static_cast<uint32_t>(bf16_bits(acc[c8 * 8 + 3])) << 16);
+      w.z = bf16_bits(acc[c8 * 8 + 4]) | (static_cast<uint32_t>(bf16_bits(acc[c8 * 8 + 5])) << 16);
+      w.w = bf16_bits(acc[c8 * 8 + 6]) | (static_cast<uint32_t>(bf16_bits(acc[c8 * 8 + 7])) << 16);
+      *reinterpret_cast<uint4*>(bout + (c8 * 16 + (tid >> 3)) * 64 + (tid & 7) * 8) = w;
+    }
+  }
   const float sc = which == 0 ? p.qscale : 1.f;
 #pragma unroll
   for (int k = 0; k < MP; ++k) acc[k] *= sc;
 
   uint16_t vals[KD];
-  if constexpr (MODE == ProjOut::BF16X1) {
-#pragma unroll
-    for (int k = 0; k < MP; ++k) vals[k] = bf16_bits(acc[k]);
-  } else if constexpr (MODE == ProjOut::F16X1) {
+  if constexpr (MODE == ProjOut::F16X1) {
     float amax = 0.f;
 #pragma unroll
     for (int k = 0; k < MP; ++k) amax = fmaxf(amax, fabsf(acc[k]));
@@ -462,17 +474,6 @@ cudaError_t launch_project(const ProjParams& p, cudaStream_t stream) {
       case 128:
         return tc ? launch_tc_mp<128, ProjOut::F16ROWS>(p, stream)
                   : launch_one<__nv_bfloat16, 128, ProjOut::F16ROWS>(p, stream);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  if (p.mode == ProjOut::BF16X1) {
-    switch (p.m) {
-      case 16:
-        return tc ? launch_tc_mp<16, ProjOut::BF16X1>(p, stream)
-                  : launch_one<__nv_bfloat16, 16, ProjOut::BF16X1>(p, stream);
-      case 32:
-        return tc ? launch_tc_mp<32, ProjOut::BF16X1>(p, stream)
-                  : launch_one<__nv_bfloat16, 32, ProjOut::BF16X1>(p, stream);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -160,12 +160,15 @@ int encode_bf16_rows(CUtensorMap* map, const void* base, int inner, int N, int B
   return encode_rows_map(map, base, inner, N, BH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2);
 }
 
-// Stage 1: projection of q and k into the workspace.
+// Stage 1: projection of q and k into the workspace (and, for the backward,
+// plain bf16 tiles of Qp and Kp into qb, kb in the same pass).
 int run_prepare(const void* q, const void* k, const void* P, int B, int H, int N, int d, int m,
-                int dtype, void* ws, cudaStream_t stream) {
+                int dtype, void* ws, cudaStream_t stream, void* qb = nullptr, void* kb = nullptr) {
   const Layout L = make_layout(B, H, N, m, dtype);
   spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, dtype, L, static_cast<char*>(ws));
   pp.use_tc = 1;
+  pp.out_b16[0] = qb;
+  pp.out_b16[1] = kb;
   if (spa::project_tc_eligible(pp)) {
     int st;
     if ((st = encode_bf16_rows(&pp.xmap[0], q, d, N, B * H))) return st;
@@ -368,11 +371,11 @@ int host_forward(const char* q, const char* k, const char* v, const char* P, flo
 // Workspace of the fused backward: the forward's prepared operands (so that
 // the recomputed scores are bit-identical to the forward's), bf16 Qp / Kp
 // tiles for the gradient products, the row statistics, the dQp accumulator,
-// dKp, their bf16 hi | lo rows, [P_h | P_h], the projection-gradient partial
+// the bf16 hi | lo rows of dQp and dKp, [P_h | P_h], the projection-gradient partial
 // R, and (when the caller has no log-sum-exp) lse plus a scratch output.
 struct BwdLayout {
   Layout fwd;
-  size_t qb = 0, kb = 0, stats = 0, dqacc = 0, dkp = 0, xq = 0, xk = 0, p2 = 0, R = 0;
+  size_t qb = 0, kb = 0, stats = 0, dqacc = 0, xq = 0, xk = 0, p2 = 0, R = 0;
   size_t lse = 0, out2 = 0, total = 0;
 };
 
@@ -390,7 +393,6 @@ BwdLayout make_bwd_layout(int B, int H, int N, int d, int m, int dv, bool own_ls
   L.kb = take(rows * m * 2);
   L.stats = take(rows * 4 * sizeof(float));
   L.dqacc = take(rows * m * sizeof(float));
-  L.dkp = take(BH * N * m * sizeof(float));
   L.xq = take(BH * N * 2 * m * 2);
   L.xk = take(BH * N * 2 * m * 2);
   L.p2 = take(static_cast<size_t>(H) * d * 2 * m * 2);
@@ -408,27 +410,14 @@ bool bwd_fused_eligible(int m, int dv, int dtype) {
 }
 
 // Fused backward, stage 1 on a workspace laid out by make_bwd_layout, after
-// run_prepare has put the forward's score operands at its start: the bf16
-// Qp / Kp tiles, the zeroed dQp accumulator and the row statistics.
-int bwd_stage_inputs(const void* q, const void* k, const void* P, const float* out,
-                     const float* lse, const void* dO, int B, int H, int N, int d, int m, int d_v,
-                     char* w, cudaStream_t stream) {
+// run_prepare (given the layout's qb / kb) has put the forward's score operands
+// and the bf16 Qp / Kp tiles in it: the zeroed dQp accumulator and the row
+// statistics.
+int bwd_stage_inputs(const float* out, const float* lse, const void* dO, int B, int H, int N,
+                     int d, int m, int d_v, char* w, cudaStream_t stream) {
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
   const int BH = B * H, NT = L.fwd.NT;
   int st;
-  spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, SPA_BF16, L.fwd, w);
-  pp.mode = ProjOut::BF16X1;
-  pp.out[0] = w + L.qb;
-  pp.out[1] = w + L.kb;
-  pp.mul[0] = pp.mul[1] = nullptr;
-  pp.qscale = 1.f;
-  pp.use_tc = 1;
-  if (spa::project_tc_eligible(pp)) {
-    if ((st = encode_bf16_rows(&pp.xmap[0], q, d, N, BH))) return st;
-    if ((st = encode_bf16_rows(&pp.xmap[1], k, d, N, BH))) return st;
-    if ((st = device_error_ptr(&pp.err))) return st;
-  }
-  if ((st = cuda_status(spa::launch_project(pp, stream)))) return st;
   const float alpha = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
   if ((st = cuda_status(cudaMemsetAsync(w + L.dqacc, 0,
                                         static_cast<size_t>(BH) * NT * spa::kTileRows * m *
@@ -458,7 +447,7 @@ int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int
   bp.Kb = reinterpret_cast<const uint16_t*>(w + L.kb);
   bp.stats = reinterpret_cast<const float*>(w + L.stats);
   bp.dqacc = reinterpret_cast<float*>(w + L.dqacc);
-  bp.dkp = reinterpret_cast<float*>(w + L.dkp);
+  bp.xk = reinterpret_cast<uint16_t*>(w + L.xk);
   bp.dv_out = dv;
   bp.BH = BH;
   bp.N = N;
@@ -482,9 +471,8 @@ int bwd_stage_finish(const void* q, const void* k, const void* P, float* dq, flo
   uint16_t* xq = reinterpret_cast<uint16_t*>(w + L.xq);
   uint16_t* xk = reinterpret_cast<uint16_t*>(w + L.xk);
   uint16_t* p2 = reinterpret_cast<uint16_t*>(w + L.p2);
-  if ((st = cuda_status(spa::launch_bwd_split(reinterpret_cast<const float*>(w + L.dqacc),
-                                              reinterpret_cast<const float*>(w + L.dkp), xq, xk,
-                                              BH, N, L.fwd.NT, m, stream))))
+  if ((st = cuda_status(spa::launch_bwd_split(reinterpret_cast<const float*>(w + L.dqacc), xq, BH,
+                                              N, L.fwd.NT, m, stream))))
     return st;
   if ((st = cuda_status(
            spa::launch_bwd_dup_p(static_cast<const __nv_bfloat16*>(P), p2, H, d, m, stream))))
@@ -501,7 +489,7 @@ int run_backward_fused(const void* q, const void* k, const void* v, const void* 
                        float* dP, int B, int H, int N, int d, int m, int d_v, int causal, char* w,
                        cudaStream_t stream) {
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, lse == nullptr);
-  int st = run_prepare(q, k, P, B, H, N, d, m, SPA_BF16, w, stream);
+  int st = run_prepare(q, k, P, B, H, N, d, m, SPA_BF16, w, stream, w + L.qb, w + L.kb);
   if (st) return st;
   if (lse == nullptr) {
     float* own = reinterpret_cast<float*>(w + L.lse);
@@ -510,7 +498,7 @@ int run_backward_fused(const void* q, const void* k, const void* v, const void* 
     if (st) return st;
     lse = own;
   }
-  if ((st = bwd_stage_inputs(q, k, P, out, lse, dO, B, H, N, d, m, d_v, w, stream))) return st;
+  if ((st = bwd_stage_inputs(out, lse, dO, B, H, N, d, m, d_v, w, stream))) return st;
   if ((st = bwd_stage_kernel(v, dO, dv, B, H, N, d, m, d_v, causal, w, stream))) return st;
   return bwd_stage_finish(q, k, P, dq, dk, dP, B, H, N, d, m, d_v, w, stream);
 }
@@ -943,8 +931,9 @@ int spa_attention_bwd_prepare(const void* q, const void* k, const void* P, const
     return SPA_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(workspace);
-  if ((st = run_prepare(q, k, P, B, H, N, d, m, SPA_BF16, w, s))) return st;
-  return bwd_stage_inputs(q, k, P, out, lse, dO, B, H, N, d, m, d_v, w, s);
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
+  if ((st = run_prepare(q, k, P, B, H, N, d, m, SPA_BF16, w, s, w + L.qb, w + L.kb))) return st;
+  return bwd_stage_inputs(out, lse, dO, B, H, N, d, m, d_v, w, s);
 }
 
 int spa_attention_bwd_apply(const void* v, const void* dO, float* dv, int B, int H, int N, int d,
