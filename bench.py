@@ -684,7 +684,9 @@ def run_backward(args, rank, world, local_rank):
                          "peak_source": f"{peak_src} bf16 burst",
                          "frac_of_sustained": achieved / peak_sus},
             "kernels_ms_per_step": {"bwd_ws_kernel": k_ms, "rest": t_ms / K - k_ms},
-            "gpu_launches": 7 * K,
+            # ours per step: projection, statistics, the kernel, dQp split,
+            # [P_h | P_h], dP fold (plus library GEMMs and one memset)
+            "gpu_launches": 6 * K,
             "clocks": clocks,
         }
         if cpu is not None:

@@ -185,3 +185,81 @@ def test_topk_and_sfa_reject_bad_arguments(lib):
     assert sfa(A, A, A, A, 1, 2, 64, 128, 128, 0, 0, BF16, None) == SHAPE
     assert sfa(A, None, A, A, 1, 2, 64, 128, 128, 8, 0, BF16, None) == NULL
     assert sfa(None, None, None, None, 1, 2, 0, 128, 128, 8, 0, BF16, None) == OK
+
+
+def test_forward_lse_validates_first(lib):
+    def f(lse=A, **kw):
+        a = dict(q=A, k=A, v=A, P=A, out=A, B=1, H=2, N=256, d=128, m=32, dv=128, causal=1,
+                 dtype=BF16)
+        a.update(kw)
+        return lib.spa_attention_fwd_lse(a["q"], a["k"], a["v"], a["P"], a["out"], lse, a["B"],
+                                         a["H"], a["N"], a["d"], a["m"], a["dv"], a["causal"],
+                                         a["dtype"], None)
+    assert f(lse=None) == NULL
+    assert f(lse=A + 2) == ALIGN
+    assert f(q=None) == NULL
+    assert f(N=-1) == SHAPE
+    assert f(N=0, lse=None) == OK  # empty: nothing to write
+
+
+def bwd_lse(lib, lse=A, dO=A, dq=A, dk=A, dv_=A, dP=A, B=1, H=2, N=256, d=128, m=32, dv=128,
+            dtype=BF16):
+    return lib.spa_attention_bwd_lse(A, A, A, A, A, lse, dO, dq, dk, dv_, dP, B, H, N, d, m, dv,
+                                     1, dtype, None)
+
+
+def test_backward_entry_points_validate_first(lib):
+    assert bwd_lse(lib, lse=None) == NULL          # the _lse form needs the log-sum-exp
+    assert bwd_lse(lib, dq=None) == NULL
+    assert bwd_lse(lib, N=-3) == SHAPE
+    assert bwd_lse(lib, d=192) == UNSUPPORTED     # d <= 128 for both backward versions
+    assert bwd_lse(lib, dO=A + 8) == ALIGN        # the fused path loads dO with TMA
+    assert bwd_lse(lib, N=0, dP=None) == NULL     # empty problem: dP is still zeroed
+    # spa_attention_bwd (no lse) checks the same way
+    assert lib.spa_attention_bwd(A, A, A, A, A, A, A, A, A, None, 1, 2, 256, 128, 32, 128, 1, BF16,
+                                 None) == NULL
+
+
+def bwd_ws_size(lib, B=1, H=2, N=256, d=128, m=32, dv=128, dtype=BF16):
+    n = ctypes.c_size_t(12345)
+    st = lib.spa_attention_bwd_workspace_size(B, H, N, d, m, dv, dtype, ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("m", [16, 32])
+def test_backward_workspace_size(lib, m):
+    st, small = bwd_ws_size(lib, N=256, m=m)
+    assert st == OK
+    st, big = bwd_ws_size(lib, N=4096, m=m)
+    assert st == OK and big > small
+    # at least the forward's operands, the bf16 tiles, statistics, dQp
+    # accumulator and hi|lo rows of the problem (N = 4096, B*H = 2)
+    rows = 2 * 4096
+    KD = 3 * m if m == 16 else m
+    assert big >= rows * (2 * 2 * KD + 4 + 2 * 2 * m + 16 + 4 * m + 2 * 2 * 2 * m)
+
+
+def test_backward_workspace_size_rejects(lib):
+    assert bwd_ws_size(lib, m=64)[0] == UNSUPPORTED   # outside the fused TMEM plan
+    assert bwd_ws_size(lib, dtype=F32)[0] == UNSUPPORTED
+    assert bwd_ws_size(lib, dv=96)[0] == UNSUPPORTED
+    assert bwd_ws_size(lib, N=0) == (OK, 0)
+    assert lib.spa_attention_bwd_workspace_size(1, 1, 8, 64, 32, 64, BF16, None) == NULL
+
+
+def test_backward_stages_check_their_workspace(lib):
+    st, need = bwd_ws_size(lib)
+    prep = lambda ws, nb, m=32: lib.spa_attention_bwd_prepare(A, A, A, A, A, A, 1, 2, 256, 128, m,
+                                                              128, BF16, ws, nb, None)
+    assert prep(None, need) == NULL
+    assert prep(A + 16, need) == ALIGN      # 256-byte alignment for the workspace
+    assert prep(A, need - 1) == NOMEM
+    assert prep(A, need, m=64) == UNSUPPORTED
+    app = lambda ws, nb: lib.spa_attention_bwd_apply(A, A, A, 1, 2, 256, 128, 32, 128, 1, BF16,
+                                                     ws, nb, None)
+    assert app(None, need) == NULL
+    assert app(A, 16) == NOMEM
+    fin = lambda dP: lib.spa_attention_bwd_finish(A, A, A, A, A, dP, 1, 2, 256, 128, 32, 128, BF16,
+                                                  A, need, None)
+    assert fin(None) == NULL
+    assert fin(A + 4) == ALIGN
