@@ -335,6 +335,16 @@ SPA_API int spa_sfa_attention_fwd(const void *q, const void *k, const void *v, f
 SPA_API int spa_selftest_wait_timeout(int limit_ms);
 
 /*
+ * spa_selftest_bwd_wait_timeout -- the same self-test for the fused backward
+ * kernel: one small causal backward (B=1 H=1 N=256 d=64 m=32 d_v=64, zero
+ * inputs) whose first "scores ready" arrival is withheld and whose waits are
+ * limited to limit_ms (1..2000).  Returns SPA_ERR_TIMEOUT when the kernel
+ * reported the timeout (the expected outcome), SPA_OK when it did not, or
+ * another status if a call failed.  The device stays usable afterwards.
+ */
+SPA_API int spa_selftest_bwd_wait_timeout(int limit_ms);
+
+/*
  * spa_device_error -- reads and clears the device error word of the current
  * device (synchronising it first).  *code receives 0 when no kernel gave up
  * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.

@@ -46,6 +46,8 @@ lib.spa_device_error.argtypes = [ctypes.POINTER(_i)]
 lib.spa_device_error.restype = _i
 lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
+lib.spa_selftest_bwd_wait_timeout.argtypes = [_i]
+lib.spa_selftest_bwd_wait_timeout.restype = _i
 lib.spa_attention_bwd.argtypes = [_vp] * 10 + [_i] * 8 + [_vp]
 lib.spa_attention_bwd.restype = _i
 lib.spa_host_pool_trim.argtypes = []
@@ -354,6 +356,11 @@ def selftest_wait_timeout(limit_ms: int = 50) -> int:
     """Run the failure-detection self-test; returns the spa_status code
     (SPA_ERR_TIMEOUT when the withheld barrier was detected, as expected)."""
     return int(lib.spa_selftest_wait_timeout(int(limit_ms)))
+
+
+def selftest_bwd_wait_timeout(limit_ms: int = 50) -> int:
+    """The same self-test for the fused backward kernel (returns the status code)."""
+    return int(lib.spa_selftest_bwd_wait_timeout(int(limit_ms)))
 
 
 def device_error() -> int:

@@ -228,12 +228,16 @@ __device__ __forceinline__ void bwd_issuer(const BwdTcParams& p, uint32_t sbase,
     dDoK[s] = smem_desc(st + Plan::kStDo, 16, 1024, kLayoutSwizzle128);
     dDoM[s] = smem_desc(st + Plan::kStDo, 16384, 1024, kLayoutSwizzle128);
   }
+  bool first_s = true;
   auto issue_s = [&](int s) {  // S^T = Kf Qf^T
     const uint64_t b = s ? dQf[1] : dQf[0];
 #pragma unroll
     for (int k = 0; k < KD / 16; ++k)
       mma_ss(tb + Plan::kColS, dKf + (k * 4096 >> 4), b + (k * 4096 >> 4), kIdS, k > 0);
-    mma_commit(&bars.s_full);
+    // a failure-detection test withholds the CTA's first "S^T ready": the
+    // gradient warpgroups' wait for it runs out, and every role takes its abort path
+    if (!(p.inject_stall && first_s)) mma_commit(&bars.s_full);
+    first_s = false;
   };
   auto issue_dp = [&](int s) {  // dP^T = V dO^T, depth d_v
     const uint64_t b = s ? dDoK[1] : dDoK[0];

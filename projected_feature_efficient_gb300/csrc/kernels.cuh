@@ -113,7 +113,8 @@ struct BwdTcParams {
   int BH, N, NT, KD, m, dv, causal;
   int f16_ops;           // 1: fp16 score operands, 0: bf16 (split) score operands
   float alpha;           // 1/sqrt(m)
-  unsigned long long limit_ns;
+  unsigned long long limit_ns;  // time limit of every wait in the kernel
+  int inject_stall;      // failure-detection test only: withhold one barrier arrival
 };
 bool bwd_tc_supported(int m, int dv);
 cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream);

@@ -432,7 +432,8 @@ int bwd_stage_inputs(const float* out, const float* lse, const void* dO, int B, 
 
 // Fused backward, stage 2: the tensor-core kernel (dV, dKp, dQp).
 int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int N, int d, int m,
-                     int d_v, int causal, char* w, cudaStream_t stream) {
+                     int d_v, int causal, char* w, cudaStream_t stream,
+                     unsigned long long limit_ns = kWaitLimitNs, int inject_stall = 0) {
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
   const int BH = B * H;
   int st;
@@ -458,7 +459,8 @@ int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int
   bp.causal = causal != 0;
   bp.f16_ops = L.fwd.mode == ProjOut::F16X1;
   bp.alpha = static_cast<float>(1.0 / std::sqrt(static_cast<double>(m)));
-  bp.limit_ns = kWaitLimitNs;
+  bp.limit_ns = limit_ns;
+  bp.inject_stall = inject_stall;
   return cuda_status(spa::launch_bwd_tc(bp, stream));
 }
 
@@ -998,6 +1000,49 @@ int spa_selftest_wait_timeout(int limit_ms) {
   if (!st)
     st = run_apply(buf + ov, reinterpret_cast<float*>(buf + oo), B, H, N, m, dv, 0, SPA_BF16,
                    buf + ow, nullptr, static_cast<unsigned long long>(limit_ms) * 1000000ull, 1);
+  if (!st) st = cuda_status(cudaDeviceSynchronize());
+  int word = 0;
+  if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  if (!st) st = cuda_status(cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  cudaFree(buf);
+  if (st) return st;
+  return word ? SPA_ERR_TIMEOUT : SPA_OK;
+}
+
+int spa_selftest_bwd_wait_timeout(int limit_ms) {
+  if (limit_ms <= 0 || limit_ms > 2000) return SPA_ERR_SHAPE;
+  constexpr int B = 1, H = 1, N = 256, d = 64, m = 32, dv = 64;
+  const size_t nq = static_cast<size_t>(N) * d * 2, nv = static_cast<size_t>(N) * dv * 2;
+  const size_t np = static_cast<size_t>(d) * m * 2, no = static_cast<size_t>(N) * dv * 4;
+  const size_t nl = static_cast<size_t>(N) * 4;
+  const size_t oq = 0, ok = align256(oq + nq), ov = align256(ok + nq), op = align256(ov + nv),
+               odo = align256(op + np), oo = align256(odo + nv), ol = align256(oo + no),
+               odv = align256(ol + nl), ow = align256(odv + no);
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, dv, false);
+  const size_t total = ow + L.total;
+  int* err = nullptr;
+  int st = device_error_ptr(&err);
+  if (st) return st;
+  char* buf = nullptr;
+  if (cudaMalloc(reinterpret_cast<void**>(&buf), total) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  // zero inputs and log-sum-exp: every value the kernel computes is finite
+  st = cuda_status(cudaMemset(buf, 0, total));
+  char* w = buf + ow;
+  if (!st)
+    st = run_prepare(buf + oq, buf + ok, buf + op, B, H, N, d, m, SPA_BF16, w, nullptr, w + L.qb,
+                     w + L.kb);
+  if (!st)
+    st = bwd_stage_inputs(reinterpret_cast<const float*>(buf + oo),
+                          reinterpret_cast<const float*>(buf + ol), buf + odo, B, H, N, d, m, dv, w,
+                          nullptr);
+  if (!st)
+    st = bwd_stage_kernel(buf + ov, buf + odo, reinterpret_cast<float*>(buf + odv), B, H, N, d, m,
+                          dv, 1, w, nullptr, static_cast<unsigned long long>(limit_ms) * 1000000ull,
+                          1);
   if (!st) st = cuda_status(cudaDeviceSynchronize());
   int word = 0;
   if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));

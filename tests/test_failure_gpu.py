@@ -32,3 +32,31 @@ def test_withheld_barrier_is_reported_and_the_device_stays_usable():
     ref = oracle.attention(q, k, v, P, causal=False)
     assert_parity(got, ref, w.dtype, "after the self-test")
     assert pkg.device_error() == 0
+
+
+def test_backward_kernel_reports_a_withheld_barrier():
+    """The fused backward kernel's bounded waits: its first "scores ready" is
+    withheld, the gradient warpgroups give up after 50 ms, every role (the
+    copy thread, the issuer, the epilogue warpgroup with its named barriers)
+    leaves through its abort path, and the device error word reports it.  A full backward afterwards is still correct."""
+    pkg = spa()
+    assert pkg.device_error() == 0
+    t0 = time.perf_counter()
+    status = pkg.selftest_bwd_wait_timeout(50)
+    elapsed = time.perf_counter() - t0
+    assert status == pkg.SPA_ERR_TIMEOUT, pkg.status_str(status)
+    assert elapsed < 1.5, f"self-test took {elapsed:.2f} s"
+    assert pkg.device_error() == 0
+    w = si.WORKLOADS["C3"].scaled(B=1, H=2, N=200, d=64, m=32, dv=64)
+    q, k, v = si.make_qkv(w, seed=5)
+    P = si.make_P(w, seed=6)
+    dO = torch.randn((1, 2, 200, 64), generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    q_, k_, v_, P_, dO_ = (x.cuda() for x in (q, k, v, P, dO))
+    out = pkg.spa_attention_fwd(q_, k_, v_, P_, causal=True)
+    got = pkg.spa_attention_bwd(q_, k_, v_, P_, out, dO_, causal=True)
+    ref = oracle.attention_bwd(q, k, v, P, dO, causal=True)
+    for gg, rr in zip(got, ref):
+        g = gg.cpu().numpy().astype("float64")
+        rel = ((g - rr) ** 2).sum() ** 0.5 / ((rr ** 2).sum() ** 0.5)
+        assert rel < 1e-2
+    assert pkg.device_error() == 0
