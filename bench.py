@@ -12,6 +12,7 @@ and its fraction of the measured bf16 tensor-core peak.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --decode     (the decode row: projected key cache, workload D1)
     python bench.py --backward   (the backward row, workload C3)
+    python bench.py --sfa        (the Sparse Feature Attention row, C4 shape)
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent problems, no data-path collective: weak scaling); rank 0 prints
@@ -656,14 +657,19 @@ def run_backward(args, rank, world, local_rank):
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         import oracle
-        hs = 1
-        t0 = time.perf_counter()
-        oracle.attention_bwd(q_h[:1, :hs, :2048], k_h[:1, :hs, :2048], v_h[:1, :hs, :2048],
-                             P_h[:hs], dO_h[:1, :hs, :2048], causal=w.causal)
-        dt = time.perf_counter() - t0
-        cpu = {"value": bwd_flops(1, hs, 2048, d, m, dv, w.causal) / dt / 1e12, "unit": UNIT,
+        # whole heads of batch entry 0 at the full N, as many as fit the budget
+        done, dt = 0, 0.0
+        while done < H and (done == 0 or dt * (done + 1) / done <= args.cpu_seconds):
+            h = done
+            t0 = time.perf_counter()
+            oracle.attention_bwd(q_h[:1, h:h + 1], k_h[:1, h:h + 1], v_h[:1, h:h + 1],
+                                 P_h[h:h + 1], dO_h[:1, h:h + 1], causal=w.causal)
+            dt += time.perf_counter() - t0
+            done += 1
+        cpu = {"value": bwd_flops(1, done, N, d, m, dv, w.causal) / dt / 1e12, "unit": UNIT,
                "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": f"{hs} head, the first 2048 positions (causal), all gradients; {dt:.1f} s"}
+               "sample": f"{done} of {B * H} (batch, head) pairs at the full N={N} (causal), all "
+                         f"gradients; {dt:.1f} s"}
     if rank == 0:
         peak, peak_sus, peak_src = load_peaks()
         achieved = bwd_kernel_flops(B, H, N, m, dv, w.causal) / (k_ms * 1e-3) / 1e12
@@ -687,6 +693,125 @@ def run_backward(args, rank, world, local_rank):
             # ours per step: projection, statistics, the kernel, dQp split,
             # [P_h | P_h], dP fold (plus library GEMMs and one memset)
             "gpu_launches": 6 * K,
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+SFA_METRIC = "sparse-feature attention fwd TFLOP/s, dense-equivalent (2 B H N^2 (d + d_v))"
+
+
+def sfa_flops(B, H, N, d, dv, causal) -> float:
+    """The dense attention's FLOPs at the full width d (the SFA notes quote
+    speedups against it): 2 B H N^2 (d + d_v), halved if causal."""
+    return 2.0 * B * H * N * N * (d + dv) * (0.5 if causal else 1.0)
+
+
+def run_sfa(args, rank, world, local_rank):
+    """The SFA row: Top-k (k = 16 of d = 128) of every query and key row, then
+    the forward on the sparsified rows at scale 1/sqrt(d), on the C4 shape
+    (B=1 H=32 N=32768 d=128 d_v=128 bf16, full attention); inputs resident.
+    The Top-k kernel is also timed alone against the measured HBM bandwidth."""
+    import torch
+    import torch.distributed as dist
+
+    import projected_feature_efficient_gb300 as spa
+    import spa_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = si.WORKLOADS["C4"]
+    if args.heads:
+        w = w.scaled(H=args.heads)
+    B, H, N, d, dv, topk = w.B, w.H, w.N, w.d, w.dv, 16
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + w.number + 7919 * rank)
+    q = torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, H, N, dv), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    ysel = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    W = max(3, args.warmup)
+    for _ in range(W):
+        spa.spa_sfa_attention_fwd(q, k, v, topk, out=out)
+        spa.spa_topk_features(q, topk, out=ysel)
+    barrier()
+    K = args.steps
+    sampler = ClockSampler(physical_device(local_rank))
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    barrier()
+    sampler.mark_start()
+    ev[0].record(stream)
+    for _ in range(K):
+        spa.spa_sfa_attention_fwd(q, k, v, topk, out=out)
+    ev[1].record(stream)
+    for _ in range(K):
+        spa.spa_topk_features(q, topk, out=ysel)
+    ev[2].record(stream)
+    barrier()
+    sampler.mark_end()
+    clocks = sampler.summary()
+    sampler.stop()
+    t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
+    tk_ms = ev[1].elapsed_time(ev[2]) / K
+    fl = sfa_flops(B, H, N, d, dv, w.causal)
+    value = world * fl * K / (t_ms * 1e-3) / 1e12
+    if spa.device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        # head 0 at the full N: Top-k of every key row, then query rows (each
+        # against all N keys, with its own Top-k) until the budget is spent
+        qh, kh, vh = (t[0:1, 0:1].cpu() for t in (q, k, v))
+        eye = torch.eye(d, dtype=torch.bfloat16).unsqueeze(0)
+        t0 = time.perf_counter()
+        ks = torch.from_numpy(oracle.topk_features(kh, topk)).to(torch.bfloat16)
+        qs = torch.from_numpy(oracle.topk_features(qh, topk)).to(torch.bfloat16)
+        dt = time.perf_counter() - t0
+        rows, step = 0, 256
+        while rows < N and dt < args.cpu_seconds:
+            t0 = time.perf_counter()
+            oracle.attention(qs, ks, vh, eye, causal=w.causal, rows=list(range(rows, rows + step)))
+            dt += time.perf_counter() - t0
+            rows += step
+        cpu = {"value": sfa_flops(1, 1, N, d, dv, w.causal) * rows / N / dt / 1e12, "unit": UNIT,
+               "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"head 0: Top-k of all {N} key and query rows, then {rows} query rows "
+                         f"against all keys; {dt:.1f} s"}
+    if rank == 0:
+        hbm = load_hbm_peak()
+        tk_gbs = 2.0 * q.numel() * 2 / (tk_ms * 1e-3) / 1e9
+        line = {
+            "metric": SFA_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": t_ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"SFA on the C4 shape: B={B} H={H} N={N} d={d} d_v={dv} "
+                                   f"bf16, Top-k k={topk} of q and k rows, full attention",
+                       "api": "spa_sfa_attention_fwd", "l2": "inputs (805 MB) exceed L2",
+                       "parallelism": f"dp{world}"},
+            "roofline": {"bound": "hbm", "achieved": tk_gbs, "peak": hbm[0], "unit": "GB/s",
+                         "frac": tk_gbs / hbm[0], "traffic": None,
+                         "kernel": "topk_rows_kernel (reads and writes q: 2 x 2 bytes per value)",
+                         "peak_source": hbm[1]},
+            "kernels_ms_per_step": {"topk_q": tk_ms, "rest": t_ms / K - tk_ms},
+            "gpu_launches": 5 * K,  # Top-k of q and k, P = I, projection, attention
             "clocks": clocks,
         }
         if cpu is not None:
@@ -727,6 +852,8 @@ def main(argv=None):
                     help="projection width of the C4 sweep")
     ap.add_argument("--decode", action="store_true",
                     help="measure the decode row (projected key cache, workload D1) instead")
+    ap.add_argument("--sfa", action="store_true",
+                    help="measure the Sparse Feature Attention row (C4 shape, k=16) instead")
     ap.add_argument("--backward", action="store_true",
                     help="measure the backward row (workload C3) instead")
     ap.add_argument("--decode-batch", type=int, default=None,
@@ -741,6 +868,8 @@ def main(argv=None):
         return run_decode(args, rank, world, local_rank)
     if args.backward:
         return run_backward(args, rank, world, local_rank)
+    if args.sfa:
+        return run_sfa(args, rank, world, local_rank)
     return run_ours(args, rank, world, local_rank)
 
 
