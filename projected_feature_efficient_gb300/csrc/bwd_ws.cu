@@ -14,9 +14,9 @@
 // its key rows in tensor memory, and adds each query tile's share of dQp into
 // an fp32 accumulator in global memory with a bulk reduce-add.
 //
-// Sixteen warps in four warpgroups:
-//   warps 0-7    gradient warpgroups.  TMEM lane = key row of the item's tile;
-//                warpgroup g takes query columns 64g .. 64g+63.
+// Twenty-four warps in six warpgroups:
+//   warps 0-15   gradient warpgroups.  TMEM lane = key row of the item's tile;
+//                warpgroup g takes query columns 32g .. 32g+31.
 //                  P-phase:  S^T -> P^T = exp2(S^T a_i - L_i log2 e), a_i the
 //                            range multipliers of the score operands; bf16 P^T
 //                            written over its own S^T columns for the dV product.
@@ -24,30 +24,32 @@
 //                            bf16 dS^T written over its own dP^T columns (dKp
 //                            product) and into a shared-memory tile in the
 //                            MN-major layout the dQp product reads (dS, M = queries).
-//   warps 8-11   epilogue: per query tile the column factors a_i, then the
+//   warps 16-19  epilogue: per query tile the column factors a_i, then the
 //                dQp tile out of TMEM, through a staging tile, into the
 //                reduce-add; per item the dV rows (fp32) and the dKp rows
 //                (bf16 hi | lo pairs, what the projection-gradient GEMMs read).
-//   warp 12      loads (one thread): per item the key tile's score operand,
+//   warp 20      loads (one thread): per item the key tile's score operand,
 //                its bf16 Kp tile and V; per query tile a two-slot ring of
 //                dO, the score operand, the bf16 Qp tile and the row statistics.
-//   warp 13      tensor-memory allocation and tcgen05.mma issue (one thread).
-//   warps 14-15  idle.
+//   warp 21      tensor-memory allocation; one thread issues S^T, dV and dQp.
+//   warp 22      one thread issues dP^T and dKp.
+//   warp 23      idle.
 // Tensor memory (512 columns): S^T/P^T | dP^T/dS^T | dV | dKp | dQp.
-// MMA issue order per query tile i:
-//   S^T(i) = Kf Qf_i^T      (first tile of an item only; otherwise issued early)
-//   dP^T(i) = V dO_i^T
-//   dV += P^T(i) dO_i        (A from TMEM)               after the P-phase
-//   S^T(i+1)                 (overwrites P^T(i) after the dV product read it)
-//   dKp += dS^T(i) Qb_i      (A from TMEM)               after the dS-phase
-//   dQp_i = dS(i) Kb         (A from shared memory)
+// Per query tile i the two issuing threads run
+//   X: S^T(i) = Kf Qf_i^T (first tile of an item; otherwise issued early)
+//      [P-phase done]  dV += P^T(i) dO_i   (A from TMEM)
+//      S^T(i+1)        (overwrites P^T(i) after the dV product read it)
+//      [dS-phase done] dQp_i = dS(i) Kb    (A from shared memory)
+//   Y: dP^T(i) = V dO_i^T
+//      [dS-phase done] dKp += dS^T(i) Qb_i (A from TMEM)
 // so the P-phase of tile i+1 overlaps the dKp/dQp/dP products, and the
 // dS-phase of tile i overlaps the dV and next score products.  MMAs from one
 // thread execute in issue order, so an MMA that overwrites columns never
-// overtakes an earlier one reading them.
+// overtakes an earlier one of the same thread reading them, and neither
+// thread overwrites columns that the other one's products read.
 //
 // Every wait is bounded; a role that gives up sets the CTA abort flag and the
-// device error word, every role leaves its loop, the issuer and the loader
+// device error word, every role leaves its loop, the issuers and the loader
 // wait (bounded) for their own operations in flight, the bulk reduce-adds
 // finish reading shared memory, and TMEM is freed before the CTA exits.
 #include <math.h>
@@ -61,9 +63,25 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBThreads = 512;
-constexpr int kBLoadWarp = 12;
-constexpr int kBMmaWarp = 13;
+// Gradient warpgroups: each takes kGradCols of the 128 query columns of a tile.
+constexpr int kGradWGs = 4;
+constexpr int kGradCols = kTileRows / kGradWGs;
+constexpr int kBEpiWarp = 4 * kGradWGs;         // first epilogue warp
+constexpr int kBLoadWarp = kBEpiWarp + 4;
+constexpr int kBMmaWarp = kBLoadWarp + 1;
+constexpr int kBThreads = 32 * (kBMmaWarp + 2 + ((kBMmaWarp + 2) & 3 ? 4 - ((kBMmaWarp + 2) & 3) : 0));
+// Register split: the block is launched with 768 x 80 registers; the gradient
+// warpgroups give some up to the epilogue warpgroup, whose loop state and
+// TMEM reads need more (the loader / issuer warpgroup keeps 80).
+constexpr uint32_t kRegGrad = 72, kRegEpi = 112, kRegLaunch = 80;
+static_assert(kGradWGs != 4 || 128 * (kGradWGs * kRegGrad + kRegEpi + kRegLaunch) <=
+                                   kBThreads * kRegLaunch,
+              "register split exceeds the launch");
+// TMEM column of the bf16 pairs of queries 16 k .. 16 k + 15 (MMA k-step k) in
+// a region where warpgroup g writes the pairs of its queries from column C g
+__host__ __device__ constexpr uint32_t pair_col(int k) {
+  return kGradCols * (16 * k / kGradCols) + 8 * (k % (kGradCols / 16));
+}
 constexpr int kBMaxDynSmem = 227 * 1024 - 1024;
 constexpr uint32_t kEpiBar = 1;  // named barrier of the epilogue warpgroup
 
@@ -102,7 +120,7 @@ struct BwdBars {
   uint64_t s_full, p_full, dp_full, ds_full;
   uint64_t dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
-  uint64_t drain;
+  uint64_t drain[2];
 };
 
 // Work item -> (head, key tile) and its query tiles qt0 .. qt0 + nq - 1.  With
@@ -204,71 +222,72 @@ __device__ __forceinline__ void bwd_loader(const BwdTcParams& p, const CUtensorM
   }
 }
 
-// ---------------------------------------------------------------- issuer
+// ---------------------------------------------------------------- issuers
+// One thread issues an unrolled run of tcgen05.mma at about 47 clocks per MMA
+// when the product is small (N = 32) and at the tensor rate for N = 128; two
+// threads in different warps issue side by side:
+//   issuer X: S^T = Kf Qf^T, dV += P^T dO, dQp = dS Kb      (18 MMAs per tile)
+//   issuer Y: dP^T = V dO^T, dKp += dS^T Qb                 (16 MMAs per tile)
+// Each overwrite of tensor memory follows, in its own thread's order, the
+// product that read the old contents (S^T(i+1) after dV(i) on X, dP^T(i+1)
+// after dKp(i) on Y); what the two streams share goes through the gradient
+// warpgroups' barriers, and each shared release (ring stage, key tile,
+// accumulators) counts one commit from each issuer.
 template <class Plan, int KD, int MB, int DV, bool F16OPS>
-__device__ __forceinline__ void bwd_issuer(const BwdTcParams& p, uint32_t sbase, uint32_t tb,
-                                           BwdBars& bars, const WaitCtl& ctl, int items) {
-  constexpr uint32_t kIdS = idesc_f16(128, 128, F16OPS ? kFmtF16 : kFmtBF16, 0, 0);
-  constexpr uint32_t kIdDP = idesc_f16(128, 128, kFmtBF16, 0, 0);
-  constexpr uint32_t kIdDV = idesc_f16(128, DV, kFmtBF16, 0, 1);
-  constexpr uint32_t kIdDK = idesc_f16(128, MB, kFmtBF16, 0, 1);
-  constexpr uint32_t kIdDQ = idesc_f16(128, MB, kFmtBF16, 1, 1);
+struct BwdDescs {
+  static constexpr uint32_t kIdS = idesc_f16(128, 128, F16OPS ? kFmtF16 : kFmtBF16, 0, 0);
+  static constexpr uint32_t kIdDP = idesc_f16(128, 128, kFmtBF16, 0, 0);
+  static constexpr uint32_t kIdDV = idesc_f16(128, DV, kFmtBF16, 0, 1);
+  static constexpr uint32_t kIdDK = idesc_f16(128, MB, kFmtBF16, 0, 1);
+  static constexpr uint32_t kIdDQ = idesc_f16(128, MB, kFmtBF16, 1, 1);
   // K-major interleaved score operands; K-major SW128 V / dO (score-like use);
   // MN-major SW128 dO (value-like use) and dS; MN-major interleaved bf16 Qp / Kp
-  const uint64_t dKf = smem_desc(sbase + Plan::kKf, 2048, 128, kLayoutInterleave);
-  const uint64_t dKb = smem_desc(sbase + Plan::kKb, 128, 2048, kLayoutInterleave);
-  const uint64_t dVk = smem_desc(sbase + Plan::kV, 16, 1024, kLayoutSwizzle128);
-  const uint64_t dDs = smem_desc(sbase + Plan::kDs, 16384, 1024, kLayoutSwizzle128);
-  uint64_t dQf[2], dQb[2], dDoK[2], dDoM[2];
+  uint64_t Kf, Kb, Vk, Ds, Qf[2], Qb[2], DoK[2], DoM[2];
+  __device__ __forceinline__ explicit BwdDescs(uint32_t sbase) {
+    Kf = smem_desc(sbase + Plan::kKf, 2048, 128, kLayoutInterleave);
+    Kb = smem_desc(sbase + Plan::kKb, 128, 2048, kLayoutInterleave);
+    Vk = smem_desc(sbase + Plan::kV, 16, 1024, kLayoutSwizzle128);
+    Ds = smem_desc(sbase + Plan::kDs, 16384, 1024, kLayoutSwizzle128);
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const uint32_t st = sbase + Plan::kRing + s * Plan::kStageBytes;
-    dQf[s] = smem_desc(st + Plan::kStQf, 2048, 128, kLayoutInterleave);
-    dQb[s] = smem_desc(st + Plan::kStQb, 128, 2048, kLayoutInterleave);
-    dDoK[s] = smem_desc(st + Plan::kStDo, 16, 1024, kLayoutSwizzle128);
-    dDoM[s] = smem_desc(st + Plan::kStDo, 16384, 1024, kLayoutSwizzle128);
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t st = sbase + Plan::kRing + s * Plan::kStageBytes;
+      Qf[s] = smem_desc(st + Plan::kStQf, 2048, 128, kLayoutInterleave);
+      Qb[s] = smem_desc(st + Plan::kStQb, 128, 2048, kLayoutInterleave);
+      DoK[s] = smem_desc(st + Plan::kStDo, 16, 1024, kLayoutSwizzle128);
+      DoM[s] = smem_desc(st + Plan::kStDo, 16384, 1024, kLayoutSwizzle128);
+    }
   }
+};
+
+template <class Plan, int KD, int MB, int DV, bool F16OPS>
+__device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbase, uint32_t tb,
+                                             BwdBars& bars, const WaitCtl& ctl, int items) {
+  using D = BwdDescs<Plan, KD, MB, DV, F16OPS>;
+  const D dsc(sbase);
   bool first_s = true;
   auto issue_s = [&](int s) {  // S^T = Kf Qf^T
-    const uint64_t b = s ? dQf[1] : dQf[0];
+    const uint64_t b = s ? dsc.Qf[1] : dsc.Qf[0];
 #pragma unroll
     for (int k = 0; k < KD / 16; ++k)
-      mma_ss(tb + Plan::kColS, dKf + (k * 4096 >> 4), b + (k * 4096 >> 4), kIdS, k > 0);
+      mma_ss(tb + Plan::kColS, dsc.Kf + (k * 4096 >> 4), b + (k * 4096 >> 4), D::kIdS, k > 0);
     // a failure-detection test withholds the CTA's first "S^T ready": the
     // gradient warpgroups' wait for it runs out, and every role takes its abort path
     if (!(p.inject_stall && first_s)) mma_commit(&bars.s_full);
     first_s = false;
   };
-  auto issue_dp = [&](int s) {  // dP^T = V dO^T, depth d_v
-    const uint64_t b = s ? dDoK[1] : dDoK[0];
-#pragma unroll
-    for (int k = 0; k < DV / 16; ++k) {
-      const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-      mma_ss(tb + Plan::kColDP, dVk + off, b + off, kIdDP, k > 0);
-    }
-    mma_commit(&bars.dp_full);
-  };
   auto issue_dv = [&](int s, uint32_t acc) {  // dV += P^T dO, depth = 128 queries
-    const uint64_t b = s ? dDoM[1] : dDoM[0];
+    const uint64_t b = s ? dsc.DoM[1] : dsc.DoM[0];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      mma_ts(tb + Plan::kColDV, tb + Plan::kColS + 64 * (k >> 2) + 8 * (k & 3),
-             b + (k * 2048 >> 4), kIdDV, k > 0 ? 1u : acc);
-  };
-  auto issue_dk = [&](int s, uint32_t acc) {  // dKp += dS^T Qb
-    const uint64_t b = s ? dQb[1] : dQb[0];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      mma_ts(tb + Plan::kColDK, tb + Plan::kColDP + 64 * (k >> 2) + 8 * (k & 3),
-             b + (k * 256 >> 4), kIdDK, k > 0 ? 1u : acc);
+      mma_ts(tb + Plan::kColDV, tb + Plan::kColS + pair_col(k), b + (k * 2048 >> 4), D::kIdDV,
+             k > 0 ? 1u : acc);
   };
   auto issue_dq = [&]() {  // dQp = dS Kb, depth = 128 keys
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      mma_ss(tb + Plan::kColDQ, dDs + (k * 2048 >> 4), dKb + (k * 256 >> 4), kIdDQ, k > 0);
+      mma_ss(tb + Plan::kColDQ, dsc.Ds + (k * 2048 >> 4), dsc.Kb + (k * 256 >> 4), D::kIdDQ, k > 0);
   };
-
-  uint32_t g = 0;  // query tiles issued so far
+  uint32_t g = 0;  // query tiles so far
   bool ok = true;
   for (int k = 0; ok; ++k) {
     const int w = item_index(k, items);
@@ -282,23 +301,20 @@ __device__ __forceinline__ void bwd_issuer(const BwdTcParams& p, uint32_t sbase,
         tc_fence_after();
         issue_s(s);
       }
-      issue_dp(s);
       if (!(ok = wait_or_abort(&bars.p_full, g & 1, ctl))) break;
-      // the first dV product of an item overwrites the accumulators: the
-      // previous item's dV and dKp must have been read out
+      // the first dV product of an item overwrites the accumulator: the
+      // previous item's dV must have been read out
       if (n == 0 && k > 0 && !(ok = wait_or_abort(&bars.acc_empty, (k - 1) & 1, ctl))) break;
       tc_fence_after();
       issue_dv(s, n > 0 ? 1u : 0u);
+      mma_commit(&bars.q_empty[s]);  // X's share of stage s (Qf, dO) is read
       if (n + 1 < it.nq) {
         const int s1 = (g + 1) & 1;
         if (!(ok = wait_or_abort(&bars.q_full[s1], ((g + 1) >> 1) & 1, ctl))) break;
         tc_fence_after();
-        issue_s(s1);
+        issue_s(s1);  // overwrites P^T(i) after dV(i), in this thread's order
       }
       if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
-      tc_fence_after();
-      issue_dk(s, n > 0 ? 1u : 0u);
-      mma_commit(&bars.q_empty[s]);  // stage s: last product reading it is issued
       if (g > 0 && !(ok = wait_or_abort(&bars.dq_empty, (g - 1) & 1, ctl))) break;
       tc_fence_after();
       issue_dq();
@@ -308,8 +324,55 @@ __device__ __forceinline__ void bwd_issuer(const BwdTcParams& p, uint32_t sbase,
     mma_commit(&bars.kv_empty);
     mma_commit(&bars.acc_full);
   }
-  mma_commit(&bars.drain);
-  mbar_wait(&bars.drain, 0, ctl.limit_ns);  // own MMAs in flight
+  mma_commit(&bars.drain[0]);
+  mbar_wait(&bars.drain[0], 0, ctl.limit_ns);  // own MMAs in flight
+}
+
+template <class Plan, int KD, int MB, int DV, bool F16OPS>
+__device__ __forceinline__ void bwd_issuer_y(const BwdTcParams& p, uint32_t sbase, uint32_t tb,
+                                             BwdBars& bars, const WaitCtl& ctl, int items) {
+  using D = BwdDescs<Plan, KD, MB, DV, F16OPS>;
+  const D dsc(sbase);
+  auto issue_dp = [&](int s) {  // dP^T = V dO^T, depth d_v
+    const uint64_t b = s ? dsc.DoK[1] : dsc.DoK[0];
+#pragma unroll
+    for (int k = 0; k < DV / 16; ++k) {
+      const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+      mma_ss(tb + Plan::kColDP, dsc.Vk + off, b + off, D::kIdDP, k > 0);
+    }
+    mma_commit(&bars.dp_full);
+  };
+  auto issue_dk = [&](int s, uint32_t acc) {  // dKp += dS^T Qb
+    const uint64_t b = s ? dsc.Qb[1] : dsc.Qb[0];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mma_ts(tb + Plan::kColDK, tb + Plan::kColDP + pair_col(k), b + (k * 256 >> 4), D::kIdDK,
+             k > 0 ? 1u : acc);
+  };
+  uint32_t g = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int w = item_index(k, items);
+    if (w < 0) break;
+    const BItem it = bwd_item(p, w);
+    if (!(ok = wait_or_abort(&bars.kv_full, k & 1, ctl))) break;
+    for (int n = 0; n < it.nq; ++n, ++g) {
+      const int s = g & 1;
+      if (!(ok = wait_or_abort(&bars.q_full[s], (g >> 1) & 1, ctl))) break;
+      tc_fence_after();
+      issue_dp(s);  // overwrites dS^T(i-1) after dKp(i-1), in this thread's order
+      if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
+      if (n == 0 && k > 0 && !(ok = wait_or_abort(&bars.acc_empty, (k - 1) & 1, ctl))) break;
+      tc_fence_after();
+      issue_dk(s, n > 0 ? 1u : 0u);
+      mma_commit(&bars.q_empty[s]);  // Y's share of stage s (dO, Qb) is read
+    }
+    if (!ok) break;
+    mma_commit(&bars.kv_empty);
+    mma_commit(&bars.acc_full);
+  }
+  mma_commit(&bars.drain[1]);
+  mbar_wait(&bars.drain[1], 0, ctl.limit_ns);
 }
 
 // ---------------------------------------------------------------- gradient warpgroups
@@ -317,12 +380,16 @@ template <class Plan>
 __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t tb, BwdBars& bars, const WaitCtl& ctl,
                                              int items, int warp, int lane) {
-  const int wg = warp >> 2;                 // query columns 64 wg .. 64 wg + 63
+  constexpr int C = kGradCols;               // query columns of this warpgroup
+  constexpr int NH = C / 32;                 // 32-column TMEM loads per phase
+  const int wg = warp >> 2;                 // query columns C wg .. C wg + C - 1
   const int r = (warp & 3) * 32 + lane;     // key row of the tile == TMEM lane
   const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-  const uint32_t tS = lane_base + Plan::kColS + 64 * wg;
-  const uint32_t tDP = lane_base + Plan::kColDP + 64 * wg;
-  const uint32_t srow = sbase + Plan::kDs + wg * 16384 + r * 128;  // this row of the dS tile
+  const uint32_t tS = lane_base + Plan::kColS + C * wg;
+  const uint32_t tDP = lane_base + Plan::kColDP + C * wg;
+  // this row of the dS tile: half (C wg) / 64, first 16-byte chunk (C wg % 64) / 8
+  const uint32_t srow = sbase + Plan::kDs + (C * wg / 64) * 16384 + r * 128;
+  const uint32_t chunk0 = static_cast<uint32_t>((C * wg) % 64 / 8);
   const uint32_t sw = static_cast<uint32_t>(r & 7);
   const uint64_t alpha2 = pack_f32x2(p.alpha, p.alpha);
   uint32_t g = 0;
@@ -336,33 +403,32 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
       const int s = g & 1;
       const int qt = it.qt0 + n;
       const float* stp = reinterpret_cast<const float*>(smem + Plan::kRing + s * Plan::kStageBytes +
-                                                        Plan::kStStat) + 64 * wg;
+                                                        Plan::kStStat) + C * wg;
       // ---- P-phase: P^T = exp2(S^T a - L log2 e), masked, bf16 over S^T
       if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars.s_full, g & 1, ctl) &&
                                              wait_or_abort(&bars.cooked[s], (g >> 1) & 1, ctl))))
         break;
       tc_fence_after();
-      uint32_t x0[32], x1[32];
-      tmem_ld32(tS, x0);
-      tmem_ld32(tS + 32, x1);
-      tmem_wait_ld();
-      // query column c (of this warpgroup's 64) is visible to key row r unless
-      // the causal mask hides it on the diagonal tile; padded key rows see nothing
-      const int cmin = !row_ok ? 64 : ((p.causal && qt == it.kt) ? r - 64 * wg : 0);
-      uint32_t pk[32];
+      uint32_t x[NH][32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NH; ++h) tmem_ld32(tS + 32 * h, x[h]);
+      tmem_wait_ld();
+      // query column c (of this warpgroup's C) is visible to key row r unless
+      // the causal mask hides it on the diagonal tile; padded key rows see nothing
+      const int cmin = !row_ok ? C : ((p.causal && qt == it.kt) ? r - C * wg : 0);
+      uint32_t pk[NH][16];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
           const int c = 32 * h + 4 * i4;
           const float4 a4 = *reinterpret_cast<const float4*>(stp + 3 * kTileRows + c);
           const float4 l4 = *reinterpret_cast<const float4*>(stp + kTileRows + c);
-          const uint32_t* xv = h == 0 ? x0 : x1;
           float y0, y1, y2, y3;
-          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(xv[4 * i4]), __uint_as_float(xv[4 * i4 + 1])),
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(x[h][4 * i4]), __uint_as_float(x[h][4 * i4 + 1])),
                                  pack_f32x2(a4.x, a4.y), pack_f32x2(l4.x, l4.y)),
                        y0, y1);
-          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(xv[4 * i4 + 2]), __uint_as_float(xv[4 * i4 + 3])),
+          unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(x[h][4 * i4 + 2]), __uint_as_float(x[h][4 * i4 + 3])),
                                  pack_f32x2(a4.z, a4.w), pack_f32x2(l4.z, l4.w)),
                        y2, y3);
           float e0 = ex2(y0), e1 = ex2(y1), e2 = ex2(y2), e3 = ex2(y3);
@@ -372,20 +438,12 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
             e2 = c + 2 < cmin ? 0.f : e2;
             e3 = c + 3 < cmin ? 0.f : e3;
           }
-          pk[16 * h + 2 * i4] = pack_bf16x2(e0, e1);
-          pk[16 * h + 2 * i4 + 1] = pack_bf16x2(e2, e3);
+          pk[h][2 * i4] = pack_bf16x2(e0, e1);
+          pk[h][2 * i4 + 1] = pack_bf16x2(e2, e3);
         }
       }
-      {
-        uint32_t lo[16], hi[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          lo[i] = pk[i];
-          hi[i] = pk[16 + i];
-        }
-        tmem_st16(tS, lo);
-        tmem_st16(tS + 16, hi);
-      }
+      for (int h = 0; h < NH; ++h) tmem_st16(tS + 16 * h, pk[h]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -397,48 +455,46 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
                                 (g == 0 || wait_or_abort(&bars.dq_full, (g - 1) & 1, ctl)))))
         break;
       tc_fence_after();
-      tmem_ld32(tDP, x0);
-      tmem_ld32(tDP + 32, x1);
-      tmem_wait_ld();
-      uint32_t dk[32];
+      // dP^T 16 columns at a time (what stays live: the P pairs, the dS pairs)
+      uint32_t dk[NH][16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int q16 = 0; q16 < 2 * NH; ++q16) {
+        const int h = q16 >> 1, o = 8 * (q16 & 1);  // pairs o .. o + 7 of half h
+        uint32_t y[16];
+        tmem_ld16(tDP + 16 * q16, y);
+        tmem_wait_ld();
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const int c = 32 * h + 4 * i4;
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const int c = 16 * q16 + 4 * i4;
           const float4 d4 = *reinterpret_cast<const float4*>(stp + 2 * kTileRows + c);
-          const uint32_t* xv = h == 0 ? x0 : x1;
           float p0, p1, p2, p3;
-          unpack_bf16x2(pk[16 * h + 2 * i4], p0, p1);
-          unpack_bf16x2(pk[16 * h + 2 * i4 + 1], p2, p3);
+          unpack_bf16x2(pk[h][o + 2 * i4], p0, p1);
+          unpack_bf16x2(pk[h][o + 2 * i4 + 1], p2, p3);
           const uint64_t u01 = fma_f32x2(
-              pack_f32x2(__uint_as_float(xv[4 * i4]), __uint_as_float(xv[4 * i4 + 1])), alpha2,
+              pack_f32x2(__uint_as_float(y[4 * i4]), __uint_as_float(y[4 * i4 + 1])), alpha2,
               pack_f32x2(d4.x, d4.y));
           const uint64_t u23 = fma_f32x2(
-              pack_f32x2(__uint_as_float(xv[4 * i4 + 2]), __uint_as_float(xv[4 * i4 + 3])), alpha2,
+              pack_f32x2(__uint_as_float(y[4 * i4 + 2]), __uint_as_float(y[4 * i4 + 3])), alpha2,
               pack_f32x2(d4.z, d4.w));
           float s0, s1, s2, s3;
           unpack_f32x2(mul_f32x2(u01, pack_f32x2(p0, p1)), s0, s1);
           unpack_f32x2(mul_f32x2(u23, pack_f32x2(p2, p3)), s2, s3);
-          dk[16 * h + 2 * i4] = pack_bf16x2(s0, s1);
-          dk[16 * h + 2 * i4 + 1] = pack_bf16x2(s2, s3);
+          dk[h][o + 2 * i4] = pack_bf16x2(s0, s1);
+          dk[h][o + 2 * i4 + 1] = pack_bf16x2(s2, s3);
         }
       }
-      {
-        uint32_t lo[16], hi[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          lo[i] = dk[i];
-          hi[i] = dk[16 + i];
-        }
-        tmem_st16(tDP, lo);
-        tmem_st16(tDP + 16, hi);
-      }
+      for (int h = 0; h < NH; ++h) tmem_st16(tDP + 16 * h, dk[h]);
       // dS (M = queries) for the dQp product: 16-byte chunk q of this key row
-      // holds queries 64 wg + 8q .. +7 and sits at chunk q ^ (r % 8)
+      // holds queries 8q .. 8q + 7 of its half and sits at chunk q ^ (r % 8)
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(srow + ((q ^ sw) << 4), dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const uint32_t q = chunk0 + 4 * h + j4;
+          st_shared_v4(srow + ((q ^ sw) << 4), dk[h][4 * j4], dk[h][4 * j4 + 1], dk[h][4 * j4 + 2],
+                       dk[h][4 * j4 + 3]);
+        }
       fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
@@ -492,21 +548,23 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
       // the four warps decide together, so that they meet the barriers below as one
       if (!(ok = named_bar_and(kEpiBar, 128, ok))) break;
       tc_fence_after();
-      uint32_t v[MB];
-      if constexpr (MB == 32) {
-        tmem_ld32(lane_base + Plan::kColDQ, v);
-      } else {
-        tmem_ld16(lane_base + Plan::kColDQ, v);
+      if (e == 0) bulk_wait_group_read<0>();  // the previous reduce has read the staging tile
+      named_bar_sync(kEpiBar, 128);
+      // 16 columns (4 chunks) at a time: TMEM -> staging row
+#pragma unroll
+      for (int c16 = 0; c16 < MB / 16; ++c16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + Plan::kColDQ + 16 * c16, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t q = static_cast<uint32_t>(4 * c16 + j);
+          st_shared_v4(stage_row + ((q ^ dsw) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
       }
-      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.dq_empty);
-      if (e == 0) bulk_wait_group_read<0>();  // the previous reduce has read the staging tile
-      named_bar_sync(kEpiBar, 128);
-#pragma unroll
-      for (int q = 0; q < kChunks; ++q)
-        st_shared_v4(stage_row + ((q ^ dsw) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       fence_proxy_async_smem();
       named_bar_sync(kEpiBar, 128);
       if (e == 0) {
@@ -522,42 +580,40 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
     tc_fence_after();
     const int row = it.kt * kTileRows + e;
     const bool wr = row < p.N;
-    {
-      uint32_t v[MB];
-      if constexpr (MB == 32) {
-        tmem_ld32(lane_base + Plan::kColDK, v);
-      } else {
-        tmem_ld16(lane_base + Plan::kColDK, v);
-      }
-      tmem_wait_ld();
-      if (wr) {  // dKp as bf16 pairs: [hi (m values) | lo (m values)]
-        uint4* dst = reinterpret_cast<uint4*>(p.xk + (static_cast<size_t>(it.bh) * p.N + row) * 2 * MB);
+    // dKp as bf16 pairs: [hi (m values) | lo (m values)], 16 columns at a time
+    uint4* kdst = reinterpret_cast<uint4*>(p.xk + (static_cast<size_t>(it.bh) * p.N + row) * 2 * MB);
 #pragma unroll
-        for (int q = 0; q < MB / 8; ++q) {
+    for (int c16 = 0; c16 < MB / 16; ++c16) {
+      uint32_t v[16];
+      tmem_ld16(lane_base + Plan::kColDK + 16 * c16, v);
+      tmem_wait_ld();
+      if (wr) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             split_pair(__uint_as_float(v[8 * q + 2 * i]), __uint_as_float(v[8 * q + 2 * i + 1]),
                        hi[i], lo[i]);
-          dst[q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          dst[MB / 8 + q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          kdst[2 * c16 + q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          kdst[MB / 8 + 2 * c16 + q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
     float4* dvrow = reinterpret_cast<float4*>(p.dv_out + (static_cast<size_t>(it.bh) * p.N + row) * DV);
 #pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(lane_base + Plan::kColDV + c0, v);
+    for (int c0 = 0; c0 < DV; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(lane_base + Plan::kColDV + c0, v);
       tmem_wait_ld();
-      if (c0 + 32 == DV) {  // every accumulator column is read: the next item may start
+      if (c0 + 16 == DV) {  // every accumulator column is read: the next item may start
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.acc_empty);
       }
       if (wr) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < 4; ++q)
           dvrow[c0 / 4 + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
       }
@@ -590,21 +646,22 @@ __global__ void __launch_bounds__(kBThreads, 1)
   }
   if (tid == 0) {
     mbar_init(&bars.kv_full, 1);
-    mbar_init(&bars.kv_empty, 1);
+    mbar_init(&bars.kv_empty, 2);  // one commit per issuer
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.q_empty[s], 2);
       mbar_init(&bars.cooked[s], 4);  // one arrival per epilogue warp
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 8);   // one arrival per gradient warp
+    mbar_init(&bars.p_full, 4 * kGradWGs);   // one arrival per gradient warp
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.ds_full, 8);
+    mbar_init(&bars.ds_full, 4 * kGradWGs);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_empty, 4);
-    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_full, 2);
     mbar_init(&bars.acc_empty, 4);
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -612,14 +669,18 @@ __global__ void __launch_bounds__(kBThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base_sh;
-  if (warp < 8) {
+  if (warp < kBEpiWarp) {
+    setmaxnreg_dec<kRegGrad>();  // every gradient warpgroup
     bwd_gradient<Plan>(p, smem, sbase, tb, bars, ctl, items, warp, lane);
-  } else if (warp < 12) {
+  } else if (warp < kBEpiWarp + 4) {
+    setmaxnreg_inc<kRegEpi>();   // the epilogue warpgroup
     bwd_epilogue<Plan, MB, DV>(p, smem, sbase, tb, bars, ctl, items, warp, lane);
   } else if (warp == kBLoadWarp) {
     if (lane == 0) bwd_loader<Plan, KD, MB, DV>(p, &vmap, &domap, smem, bars, ctl, items);
   } else if (warp == kBMmaWarp) {
-    if (lane == 0) bwd_issuer<Plan, KD, MB, DV, F16OPS>(p, sbase, tb, bars, ctl, items);
+    if (lane == 0) bwd_issuer_x<Plan, KD, MB, DV, F16OPS>(p, sbase, tb, bars, ctl, items);
+  } else if (warp == kBMmaWarp + 1) {
+    if (lane == 0) bwd_issuer_y<Plan, KD, MB, DV, F16OPS>(p, sbase, tb, bars, ctl, items);
   }
   tc_fence_before();
   __syncthreads();
