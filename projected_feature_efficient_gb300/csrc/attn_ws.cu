@@ -384,20 +384,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_id = 1 + t;  // named barrier of this warpgroup
     uint32_t sph = 0;               // s_full phase bit
     int ndone = 0;                  // output tiles written
+    auto row_mul = [&](const Item& x) {
+      return p.qmul[static_cast<size_t>(x.bh) * p.NT * kTileRows + (x.qt0 + t) * kTileRows + r];
+    };
+    float qm_next = 0.f, km_next = 0.f;
+    bool pre = false;
     for (int k = 0;; ++k) {
       const int w = item_index(k, items);
       if (w < 0) break;
       const Item it = decode_item(p, w);
       const int nkv_t = t == 0 ? it.nkv0 : it.nkv1;
-      if (nkv_t == 0) continue;  // the last pair of an odd tile count has no tile 1
+      if (nkv_t == 0) {
+        pre = false;
+        continue;
+      }
       const int qt = it.qt0 + t;
-      const int row = qt * kTileRows + r;
-      const float qm = p.qmul[static_cast<size_t>(it.bh) * p.NT * kTileRows + row];
       const float* kmul = p.kmul + static_cast<size_t>(it.bh) * p.NT;
+      const float qm = pre ? qm_next : row_mul(it);
+      const float km0 = pre ? km_next : __ldg(kmul);
+      pre = false;
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nkv_t; ++j) {
-        const float km = __ldg(kmul + j);
+        const float km = j == 0 ? km0 : __ldg(kmul + j);
         // warp-uniform outcome, so that the warp stays converged for the
         // .sync.aligned tensor-memory instructions below
         if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars.s_full[t], sph, ctl))))
@@ -495,6 +504,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full[t]);
+      }
+      if (ok) {
+        const int wn = item_index(k + 1, items);
+        if (wn >= 0) {
+          const Item itn = decode_item(p, wn);
+          if ((t == 0 ? itn.nkv0 : itn.nkv1) > 0) {
+            qm_next = row_mul(itn);
+            km_next = __ldg(p.kmul + static_cast<size_t>(itn.bh) * p.NT);
+            pre = true;
+          }
+        }
       }
       // ---- output: O / l -> out (fp32) through shared memory and TMA stores.
       // The whole warpgroup decides together, so that it meets the named
