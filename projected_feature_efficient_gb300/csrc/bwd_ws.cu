@@ -18,8 +18,9 @@
 //   warps 0-15   gradient warpgroups.  TMEM lane = key row of the item's tile;
 //                warpgroup g takes query columns 32g .. 32g+31.
 //                  P-phase:  S^T -> P^T = exp2(S^T a_i - L_i log2 e), a_i the
-//                            range multipliers of the score operands; bf16 P^T
-//                            written over its own S^T columns for the dV product.
+//                            range multipliers of the score operands; S^T is
+//                            released as soon as it is in registers, and bf16
+//                            P^T goes to its own columns for the dV product.
 //                  dS-phase: dP^T -> dS^T = P^T (dP^T / sqrt(m) - D_i / sqrt(m));
 //                            bf16 dS^T written over its own dP^T columns (dKp
 //                            product) and into a shared-memory tile in the
@@ -34,19 +35,21 @@
 //   warp 21      tensor-memory allocation; one thread issues S^T, dV and dQp.
 //   warp 22      one thread issues dP^T and dKp.
 //   warp 23      idle.
-// Tensor memory (512 columns): S^T/P^T | dP^T/dS^T | dV | dKp | dQp.
+// Tensor memory (512 columns): S^T | dP^T/dS^T | dV | dKp | dQp | P^T.
 // Per query tile i the two issuing threads run
 //   X: S^T(i) = Kf Qf_i^T (first tile of an item; otherwise issued early)
+//      [S^T(i) in registers] S^T(i+1)      (over S^T(i))
 //      [P-phase done]  dV += P^T(i) dO_i   (A from TMEM)
-//      S^T(i+1)        (overwrites P^T(i) after the dV product read it)
 //      [dS-phase done] dQp_i = dS(i) Kb    (A from shared memory)
 //   Y: dP^T(i) = V dO_i^T
 //      [dS-phase done] dKp += dS^T(i) Qb_i (A from TMEM)
-// so the P-phase of tile i+1 overlaps the dKp/dQp/dP products, and the
-// dS-phase of tile i overlaps the dV and next score products.  MMAs from one
-// thread execute in issue order, so an MMA that overwrites columns never
-// overtakes an earlier one of the same thread reading them, and neither
-// thread overwrites columns that the other one's products read.
+// so the scores of tile i+1 are ready when the gradient warpgroups finish
+// tile i, the P-phase of tile i+1 overlaps the dKp/dQp/dP products, and the
+// dS-phase of tile i overlaps the dV product.  The gradient warpgroups store
+// P^T(i+1) only after the dV product of tile i has read P^T(i) (dv_done).
+// MMAs from one thread execute in issue order, so an MMA that overwrites
+// columns never overtakes an earlier one of the same thread reading them, and
+// neither thread overwrites columns that the other one's products read.
 //
 // Every wait is bounded; a role that gives up sets the CTA abort flag and the
 // device error word, every role leaves its loop, the issuers and the loader
@@ -109,15 +112,17 @@ struct BwdPlan {
   static constexpr int kLaunch = kBytes + 1024;  // room to align the base to 1024
   static_assert(kLaunch <= kBMaxDynSmem, "backward shared-memory plan too large");
   static_assert(kVBytes % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024 alignment");
+  // S^T | dP^T/dS^T | dV | dKp | dQp | P^T (bf16 pairs: the pair of queries
+  // 2c, 2c+1 in column c, so k-step k of the dV product reads columns 8k ..)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + DV,
-                            kColDQ = 256 + DV + MB;
-  static_assert(kColDQ + MB <= 512, "tensor-memory plan too large");
+                            kColDQ = 256 + DV + MB, kColP = 256 + DV + 2 * MB;
+  static_assert(kColP + 64 <= 512, "tensor-memory plan too large");
 };
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2], cooked[2];
-  uint64_t s_full, p_full, dp_full, ds_full;
+  uint64_t s_full, s_free, p_full, dp_full, ds_full, dv_done;
   uint64_t dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
   uint64_t drain[2];
@@ -279,7 +284,7 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
     const uint64_t b = s ? dsc.DoM[1] : dsc.DoM[0];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      mma_ts(tb + Plan::kColDV, tb + Plan::kColS + pair_col(k), b + (k * 2048 >> 4), D::kIdDV,
+      mma_ts(tb + Plan::kColDV, tb + Plan::kColP + 8 * k, b + (k * 2048 >> 4), D::kIdDV,
              k > 0 ? 1u : acc);
   };
   auto issue_dq = [&]() {  // dQp = dS Kb, depth = 128 keys
@@ -301,19 +306,24 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
         tc_fence_after();
         issue_s(s);
       }
+      if (n + 1 < it.nq) {
+        // the next tile's scores as soon as the gradient warps hold S^T(i)
+        // in registers: they overwrite nothing else
+        const int s1 = (g + 1) & 1;
+        if (!(ok = wait_or_abort(&bars.s_free, g & 1, ctl) &&
+                   wait_or_abort(&bars.q_full[s1], ((g + 1) >> 1) & 1, ctl)))
+          break;
+        tc_fence_after();
+        issue_s(s1);
+      }
       if (!(ok = wait_or_abort(&bars.p_full, g & 1, ctl))) break;
       // the first dV product of an item overwrites the accumulator: the
       // previous item's dV must have been read out
       if (n == 0 && k > 0 && !(ok = wait_or_abort(&bars.acc_empty, (k - 1) & 1, ctl))) break;
       tc_fence_after();
       issue_dv(s, n > 0 ? 1u : 0u);
+      mma_commit(&bars.dv_done);     // P^T(i) is read: the P columns are free
       mma_commit(&bars.q_empty[s]);  // X's share of stage s (Qf, dO) is read
-      if (n + 1 < it.nq) {
-        const int s1 = (g + 1) & 1;
-        if (!(ok = wait_or_abort(&bars.q_full[s1], ((g + 1) >> 1) & 1, ctl))) break;
-        tc_fence_after();
-        issue_s(s1);  // overwrites P^T(i) after dV(i), in this thread's order
-      }
       if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
       if (g > 0 && !(ok = wait_or_abort(&bars.dq_empty, (g - 1) & 1, ctl))) break;
       tc_fence_after();
@@ -386,6 +396,7 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
   const int r = (warp & 3) * 32 + lane;     // key row of the tile == TMEM lane
   const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const uint32_t tS = lane_base + Plan::kColS + C * wg;
+  const uint32_t tP = lane_base + Plan::kColP + (C / 2) * wg;
   const uint32_t tDP = lane_base + Plan::kColDP + C * wg;
   // this row of the dS tile: half (C wg) / 64, first 16-byte chunk (C wg % 64) / 8
   const uint32_t srow = sbase + Plan::kDs + (C * wg / 64) * 16384 + r * 128;
@@ -413,6 +424,9 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
 #pragma unroll
       for (int h = 0; h < NH; ++h) tmem_ld32(tS + 32 * h, x[h]);
       tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_free);  // the next S^T may overwrite these columns
       // query column c (of this warpgroup's C) is visible to key row r unless
       // the causal mask hides it on the diagonal tile; padded key rows see nothing
       const int cmin = !row_ok ? C : ((p.causal && qt == it.kt) ? r - C * wg : 0);
@@ -442,8 +456,12 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
           pk[h][2 * i4 + 1] = pack_bf16x2(e2, e3);
         }
       }
+      // P^T(i-1) must have been read by its dV product before P^T(i) replaces it
+      if (!(ok = __all_sync(0xffffffffu, g == 0 || wait_or_abort(&bars.dv_done, (g - 1) & 1, ctl))))
+        break;
+      tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < NH; ++h) tmem_st16(tS + 16 * h, pk[h]);
+      for (int h = 0; h < NH; ++h) tmem_st16(tP + 16 * h, pk[h]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -653,7 +671,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
       mbar_init(&bars.cooked[s], 4);  // one arrival per epilogue warp
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 4 * kGradWGs);   // one arrival per gradient warp
+    mbar_init(&bars.s_free, 4 * kGradWGs);   // one arrival per gradient warp
+    mbar_init(&bars.p_full, 4 * kGradWGs);
+    mbar_init(&bars.dv_done, 1);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_full, 4 * kGradWGs);
     mbar_init(&bars.dq_full, 1);
