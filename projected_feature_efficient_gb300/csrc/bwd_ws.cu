@@ -121,7 +121,7 @@ struct BwdPlan {
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2], cooked[2];
+  uint64_t qa_full[2], qa_empty[2], qb_full[2], qb_empty[2], cooked[2];
   uint64_t s_full, s_free, p_full, dp_full, ds_full, dv_done;
   uint64_t dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
@@ -203,27 +203,34 @@ __device__ __forceinline__ void bwd_loader(const BwdTcParams& p, const CUtensorM
     karmed = k + 1;
     for (int n = 0; n < it.nq; ++n, ++g) {
       const int s = g & 1;
-      if (g >= 2 && !(ok = wait_or_abort(&bars.q_empty[s], ((g >> 1) - 1) & 1, ctl))) break;
+      // part A (dO, score operand, statistics) is free once the dV and dP^T
+      // products and the gradient warps are done with it; part B (the bf16
+      // Qp tile) only after the dKp product, late in the tile
       const int qt = it.qt0 + n;
       const size_t qtile = static_cast<size_t>(it.bh) * p.NT + qt;
       uint8_t* st = smem + Plan::kRing + s * Plan::kStageBytes;
-      mbar_arrive_expect_tx(&bars.q_full[s],
-                            Plan::kVBytes + Plan::kKfBytes + Plan::kBBytes + Plan::kStatBytes);
+      if (g >= 2 && !(ok = wait_or_abort(&bars.qa_empty[s], ((g >> 1) - 1) & 1, ctl))) break;
+      mbar_arrive_expect_tx(&bars.qa_full[s], Plan::kVBytes + Plan::kKfBytes + Plan::kStatBytes);
 #pragma unroll
       for (int h = 0; h < DV / 64; ++h)
         tma_load_3d(st + Plan::kStDo + h * 16384, domap, h * 64, qt * kTileRows, it.bh,
-                    &bars.q_full[s]);
-      bulk_g2s(st + Plan::kStQf, p.Qs + qtile * kTileRows * KD, Plan::kKfBytes, &bars.q_full[s]);
-      bulk_g2s(st + Plan::kStQb, p.Qb + qtile * kTileRows * MB, Plan::kBBytes, &bars.q_full[s]);
+                    &bars.qa_full[s]);
+      bulk_g2s(st + Plan::kStQf, p.Qs + qtile * kTileRows * KD, Plan::kKfBytes, &bars.qa_full[s]);
       bulk_g2s(st + Plan::kStStat, p.stats + qtile * 4 * kTileRows, Plan::kStatBytes,
-               &bars.q_full[s]);
+               &bars.qa_full[s]);
+      if (g >= 2 && !(ok = wait_or_abort(&bars.qb_empty[s], ((g >> 1) - 1) & 1, ctl))) break;
+      mbar_arrive_expect_tx(&bars.qb_full[s], Plan::kBBytes);
+      bulk_g2s(st + Plan::kStQb, p.Qb + qtile * kTileRows * MB, Plan::kBBytes, &bars.qb_full[s]);
     }
   }
   // every copy this thread started lands before the CTA's memory is released
   if (karmed > 0) mbar_wait(&bars.kv_full, (karmed - 1) & 1, ctl.limit_ns);
   for (uint32_t s = 0; s < 2; ++s) {
     const uint32_t n = g > s ? (g - s + 1) / 2 : 0;  // times stage s was armed
-    if (n > 0) mbar_wait(&bars.q_full[s], (n - 1) & 1, ctl.limit_ns);
+    if (n > 0) {
+      mbar_wait(&bars.qa_full[s], (n - 1) & 1, ctl.limit_ns);
+      mbar_wait(&bars.qb_full[s], (n - 1) & 1, ctl.limit_ns);
+    }
   }
 }
 
@@ -302,7 +309,7 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
     for (int n = 0; n < it.nq; ++n, ++g) {
       const int s = g & 1;
       if (n == 0) {
-        if (!(ok = wait_or_abort(&bars.q_full[s], (g >> 1) & 1, ctl))) break;
+        if (!(ok = wait_or_abort(&bars.qa_full[s], (g >> 1) & 1, ctl))) break;
         tc_fence_after();
         issue_s(s);
       }
@@ -311,7 +318,7 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
         // in registers: they overwrite nothing else
         const int s1 = (g + 1) & 1;
         if (!(ok = wait_or_abort(&bars.s_free, g & 1, ctl) &&
-                   wait_or_abort(&bars.q_full[s1], ((g + 1) >> 1) & 1, ctl)))
+                   wait_or_abort(&bars.qa_full[s1], ((g + 1) >> 1) & 1, ctl)))
           break;
         tc_fence_after();
         issue_s(s1);
@@ -323,7 +330,7 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
       tc_fence_after();
       issue_dv(s, n > 0 ? 1u : 0u);
       mma_commit(&bars.dv_done);     // P^T(i) is read: the P columns are free
-      mma_commit(&bars.q_empty[s]);  // X's share of stage s (Qf, dO) is read
+      mma_commit(&bars.qa_empty[s]);  // X is done with part A of stage s (Qf, dO)
       if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
       if (g > 0 && !(ok = wait_or_abort(&bars.dq_empty, (g - 1) & 1, ctl))) break;
       tc_fence_after();
@@ -368,14 +375,17 @@ __device__ __forceinline__ void bwd_issuer_y(const BwdTcParams& p, uint32_t sbas
     if (!(ok = wait_or_abort(&bars.kv_full, k & 1, ctl))) break;
     for (int n = 0; n < it.nq; ++n, ++g) {
       const int s = g & 1;
-      if (!(ok = wait_or_abort(&bars.q_full[s], (g >> 1) & 1, ctl))) break;
+      if (!(ok = wait_or_abort(&bars.qa_full[s], (g >> 1) & 1, ctl))) break;
       tc_fence_after();
       issue_dp(s);  // overwrites dS^T(i-1) after dKp(i-1), in this thread's order
-      if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
+      mma_commit(&bars.qa_empty[s]);  // Y is done with part A of stage s (dO)
+      if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl) &&
+                 wait_or_abort(&bars.qb_full[s], (g >> 1) & 1, ctl)))
+        break;
       if (n == 0 && k > 0 && !(ok = wait_or_abort(&bars.acc_empty, (k - 1) & 1, ctl))) break;
       tc_fence_after();
       issue_dk(s, n > 0 ? 1u : 0u);
-      mma_commit(&bars.q_empty[s]);  // Y's share of stage s (dO, Qb) is read
+      mma_commit(&bars.qb_empty[s]);  // part B of stage s (Qb) is read
     }
     if (!ok) break;
     mma_commit(&bars.kv_empty);
@@ -517,7 +527,10 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.ds_full);
+      if (lane == 0) {
+        mbar_arrive(&bars.ds_full);
+        mbar_arrive(&bars.qa_empty[s]);  // this warp's last read of the statistics
+      }
     }
     if (!ok) break;
   }
@@ -539,7 +552,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
   // the column factors a_i = (Q row multiplier) x (K tile multiplier) of tile gg
   auto cook = [&](uint32_t gg, const BItem& itc) -> bool {
     const int s = gg & 1;
-    if (!__all_sync(0xffffffffu, wait_or_abort(&bars.q_full[s], (gg >> 1) & 1, ctl))) return false;
+    if (!__all_sync(0xffffffffu, wait_or_abort(&bars.qa_full[s], (gg >> 1) & 1, ctl))) return false;
     float* stp = reinterpret_cast<float*>(smem + Plan::kRing + s * Plan::kStageBytes + Plan::kStStat);
     const float km = __ldg(p.kmul + static_cast<size_t>(itc.bh) * p.NT + itc.kt);
     stp[3 * kTileRows + e] = stp[e] * km;
@@ -666,8 +679,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
     mbar_init(&bars.kv_full, 1);
     mbar_init(&bars.kv_empty, 2);  // one commit per issuer
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], 2);
+      mbar_init(&bars.qa_full[s], 1);
+      mbar_init(&bars.qa_empty[s], 2 + 4 * kGradWGs);  // both issuers, every gradient warp
+      mbar_init(&bars.qb_full[s], 1);
+      mbar_init(&bars.qb_empty[s], 1);
       mbar_init(&bars.cooked[s], 4);  // one arrival per epilogue warp
     }
     mbar_init(&bars.s_full, 1);
