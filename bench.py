@@ -808,7 +808,7 @@ def run_sfa(args, rank, world, local_rank):
                        "parallelism": f"dp{world}"},
             "roofline": {"bound": "hbm", "achieved": tk_gbs, "peak": hbm[0], "unit": "GB/s",
                          "frac": tk_gbs / hbm[0], "traffic": None,
-                         "kernel": "topk_rows_kernel (reads and writes q: 2 x 2 bytes per value)",
+                         "kernel": "topk_rows_bf16_kernel (reads and writes q: 2 x 2 bytes per value)",
                          "peak_source": hbm[1]},
             "kernels_ms_per_step": {"topk_q": tk_ms, "rest": t_ms / K - tk_ms},
             "gpu_launches": 5 * K,  # Top-k of q and k, P = I, projection, attention

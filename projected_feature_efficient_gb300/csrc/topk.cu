@@ -3,10 +3,12 @@
 // coordinates of largest magnitude and zeroes the rest; attention then runs
 // on the sparsified rows at scale 1/sqrt(d)).
 //
-// One warp per row of d = 32 * E features; lane l holds the E consecutive
+// bf16 rows of up to 128 features take a thread per row and a search on bit
+// planes (below); other rows a
+// warp per row of d = 32 * E features, lane l holding the E consecutive
 // features E*l .. E*l + E - 1.  The k-th largest magnitude T is found by a
 // binary search over the magnitude's bit pattern (for non-negative floats the
-// bit pattern orders like the value), counting with warp sums.  Every
+// bit pattern orders like the value).  Every
 // feature with |x| > T is kept, and of the features with |x| == T the ones
 // with the lowest indices, as many as k still needs (a warp-wide exclusive
 // scan in index order).  The selection is made on the exact input values, so
@@ -88,6 +90,193 @@ __global__ void __launch_bounds__(256) topk_rows_kernel(const T* __restrict__ x,
   }
 }
 
+// Delta swap: exchange the bits of x selected by m with those s places above.
+__device__ __forceinline__ uint32_t delta_swap(uint32_t x, int s, uint32_t m) {
+  const uint32_t t = (x ^ (x >> s)) & m;
+  return x ^ t ^ (t << s);
+}
+// Bit b = 16h + w of a group mask stands for feature 2w + h of the group (the
+// order the bit-plane transpose leaves); `to_index_order` interleaves the two
+// halves (bit 16h + w -> bit 2w + h), `to_plane_order` undoes it.
+__device__ __forceinline__ uint32_t to_index_order(uint32_t x) {
+  x = delta_swap(x, 8, 0x0000FF00u);
+  x = delta_swap(x, 4, 0x00F000F0u);
+  x = delta_swap(x, 2, 0x0C0C0C0Cu);
+  return delta_swap(x, 1, 0x22222222u);
+}
+__device__ __forceinline__ uint32_t to_plane_order(uint32_t x) {
+  x = delta_swap(x, 1, 0x22222222u);
+  x = delta_swap(x, 2, 0x0C0C0C0Cu);
+  x = delta_swap(x, 4, 0x00F000F0u);
+  return delta_swap(x, 8, 0x0000FF00u);
+}
+// In-place transpose of the two 16 x 16 bit matrices held in the halves of
+// x[0..15] (row = word, column = bit within the half): afterwards bit c of
+// half h of x[r] is the former bit r of half h of x[c].
+__device__ __forceinline__ void transpose16x2(uint32_t (&x)[16]) {
+#pragma unroll
+  for (int level = 0; level < 4; ++level) {
+    const int s = 8 >> level;
+    const uint32_t m = level == 0 ? 0x00FF00FFu : level == 1 ? 0x0F0F0F0Fu
+                     : level == 2 ? 0x33333333u : 0x55555555u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & s) continue;
+      const uint32_t t = ((x[i] >> s) ^ x[i + s]) & m;
+      x[i + s] ^= t;
+      x[i] ^= t << s;
+    }
+  }
+}
+
+// Top-k of one bf16 row of 32 G features held by one thread, as G groups of
+// 32 features (16 words of two; sign bits may be set).  The magnitudes of a
+// group are transposed into bit planes: word b of a group becomes the mask of
+// its features whose magnitude has bit b set.  The threshold search of the
+// warp kernel then runs on masks: E holds the features whose magnitude agrees
+// with the threshold t above the current bit, Gm the ones already known to be
+// larger; count(|x| >= t | 2^b) = |Gm| + popc(E & plane_b).  Each of the 15
+// steps costs a few instructions per 32 features instead of one or more per
+// feature.  Ties at t (E at the end) are kept lowest index first, as many as
+// k - |Gm| needs, as in the warp kernel, so both give the same bits.  On
+// return keep[g] has bits w and 16 + w set for the kept features 2w and
+// 2w + 1 of group g.
+template <int G>
+__device__ __forceinline__ void select_row(uint32_t (&a)[G][16], int k, uint32_t (&keep)[G]) {
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int w = 0; w < 16; ++w) a[g][w] &= 0x7fff7fffu;
+    transpose16x2(a[g]);
+  }
+  // largest t with count(|x| >= t) >= k, bit by bit from the top, on the planes
+  uint32_t E[G], Gm[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    E[g] = 0xffffffffu;
+    Gm[g] = 0u;
+  }
+  int greater = 0;  // popc of Gm
+#pragma unroll
+  for (int b = 14; b >= 0; --b) {
+    uint32_t Eb[G];
+    int c = greater;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      Eb[g] = E[g] & a[g][b];
+      c += __popc(Eb[g]);
+    }
+    const bool set = c >= k;  // bit b of t is 1
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      Gm[g] = set ? Gm[g] : (Gm[g] | Eb[g]);
+      E[g] = set ? Eb[g] : (E[g] & ~a[g][b]);
+    }
+    greater = set ? greater : c;
+  }
+  // the ties, lowest feature index first, as many as k still needs
+  int need = k - greater;  // >= 1: fewer than k magnitudes exceed t
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const uint32_t eo = to_index_order(E[g]);
+    const int pc = __popc(eo);
+    uint32_t sel = 0u;
+    if (need >= pc) {
+      sel = eo;
+      need -= pc;
+    } else if (need > 0) {
+      uint32_t rest = eo;
+      for (int i = 0; i < need; ++i) rest &= rest - 1u;  // drop the lowest `need`
+      sel = eo & ~rest;
+      need = 0;
+    }
+    keep[g] = Gm[g] | to_plane_order(sel);
+  }
+}
+// Word w of group g (features 2w, 2w + 1) with the dropped halves zeroed.
+template <int G>
+__device__ __forceinline__ uint32_t kept_word(uint32_t v, const uint32_t (&keep)[G], int g, int w) {
+  return v & (((keep[g] >> w) & 0x00010001u) * 0xFFFFu);
+}
+
+// bf16 rows of 32 features: one thread per row, straight from global memory
+// (a row is 64 bytes, so the 16-byte loads of a warp are half coalesced).
+__global__ void __launch_bounds__(128) topk_rows32_bf16_kernel(const uint16_t* __restrict__ x,
+                                                               uint16_t* __restrict__ y,
+                                                               long long rows, int k) {
+  const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (row >= rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + row * 32);
+  uint32_t a[1][16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = __ldg(src + i);
+    a[0][4 * i] = u.x;
+    a[0][4 * i + 1] = u.y;
+    a[0][4 * i + 2] = u.z;
+    a[0][4 * i + 3] = u.w;
+  }
+  uint32_t keep[1];
+  select_row<1>(a, k, keep);
+  uint4* dst = reinterpret_cast<uint4*>(y + row * 32);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = __ldg(src + i);
+    dst[i] = make_uint4(kept_word<1>(u.x, keep, 0, 4 * i), kept_word<1>(u.y, keep, 0, 4 * i + 1),
+                        kept_word<1>(u.z, keep, 0, 4 * i + 2),
+                        kept_word<1>(u.w, keep, 0, 4 * i + 3));
+  }
+}
+
+// bf16 rows of 64 or 128 features: one thread per row, a block's 128 rows
+// (contiguous in memory) passing through shared memory with 16-byte accesses
+// that are coalesced across the block.  In shared memory 16-byte chunk c of
+// row r sits at chunk c ^ (r % 8), so that the eight threads of a quarter
+// warp (eight consecutive rows, same chunk) and eight consecutive chunks of
+// the coalesced passes both fall in eight different bank groups.
+template <int D>
+__global__ void __launch_bounds__(128) topk_rows_bf16_kernel(const uint16_t* __restrict__ x,
+                                                             uint16_t* __restrict__ y,
+                                                             long long rows, int k) {
+  constexpr int G = D / 32, V = D / 8;  // groups of 32 features, 16-byte chunks of a row
+  static_assert(V >= 8, "eight-chunk swizzle");
+  __shared__ uint4 tile[128 * V];
+  const int tid = threadIdx.x;
+  const long long row0 = static_cast<long long>(blockIdx.x) * 128;
+  const int nrows = static_cast<int>(min(128LL, rows - row0));
+  auto slot = [](int r, int c) { return r * V + (c ^ (r & 7)); };
+  const uint4* src = reinterpret_cast<const uint4*>(x + row0 * D);
+  for (int q = tid; q < nrows * V; q += 128) tile[slot(q / V, q % V)] = __ldg(src + q);
+  __syncthreads();
+  if (tid < nrows) {
+    uint32_t a[G][16];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const uint4 u = tile[slot(tid, i)];
+      const int g = i / 4, w = (i % 4) * 4;  // four chunks per group
+      a[g][w] = u.x;
+      a[g][w + 1] = u.y;
+      a[g][w + 2] = u.z;
+      a[g][w + 3] = u.w;
+    }
+    uint32_t keep[G];
+    select_row<G>(a, k, keep);
+    // read the row again rather than keep it in registers through the search
+    asm volatile("" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < V; ++i) {  // each thread rewrites only its own row's slots
+      const uint4 u = tile[slot(tid, i)];
+      const int g = i / 4, w = (i % 4) * 4;
+      tile[slot(tid, i)] = make_uint4(kept_word<G>(u.x, keep, g, w), kept_word<G>(u.y, keep, g, w + 1),
+                                      kept_word<G>(u.z, keep, g, w + 2),
+                                      kept_word<G>(u.w, keep, g, w + 3));
+    }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(y + row0 * D);
+  for (int q = tid; q < nrows * V; q += 128) dst[q] = tile[slot(q / V, q % V)];
+}
+
 template <typename T>
 cudaError_t launch_typed(const TopkParams& p, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>((p.rows + 7) / 8);
@@ -126,9 +315,26 @@ cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_bf16_rows(const TopkParams& p, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((p.rows + 127) / 128);
+  const uint16_t* x = static_cast<const uint16_t*>(p.x);
+  uint16_t* y = static_cast<uint16_t*>(p.y);
+  if constexpr (D == 32)
+    topk_rows32_bf16_kernel<<<grid, 128, 0, stream>>>(x, y, p.rows, p.k);
+  else
+    topk_rows_bf16_kernel<D><<<grid, 128, 0, stream>>>(x, y, p.rows, p.k);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
   if (p.rows > 8LL * 0x7fffffffLL) return cudaErrorInvalidValue;
+  // bf16 rows up to 128 features: a thread per row (16-byte row accesses; x
+  // and y are 16-byte aligned and every row is a multiple of 16 bytes)
+  if (p.bf16 && p.d == 128) return launch_bf16_rows<128>(p, stream);
+  if (p.bf16 && p.d == 64) return launch_bf16_rows<64>(p, stream);
+  if (p.bf16 && p.d == 32) return launch_bf16_rows<32>(p, stream);
   return p.bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);
 }
 

@@ -35,6 +35,21 @@ def test_topk_is_bit_exact(dtype, d):
         assert torch.equal(got.view(view), want.view(view)), f"d={d} k={k}"
 
 
+def test_topk_full_size_sampled():
+    """The Top-k of q at the SFA measurement's size (B=1 H=32 N=32768 d=128,
+    k=16: 2^20 rows, the launch the bench times), a third of the rows from a
+    tiny value set; sampled rows, the first and the last, bit for bit."""
+    pkg = spa()
+    rows, d, k = 1 << 20, 128, 16
+    x = rows_with_ties(rows, d, torch.bfloat16, seed=7)
+    got = pkg.spa_topk_features(x.cuda(), k).cpu()
+    g = torch.Generator().manual_seed(8)
+    idx = torch.cat([torch.tensor([0, rows // 3 - 1, rows // 3, rows - 1]),
+                     torch.randint(0, rows, (3000,), generator=g)])
+    want = torch.from_numpy(oracle.topk_features(x[idx], k)).to(torch.bfloat16)
+    assert torch.equal(got[idx].view(torch.int16), want.view(torch.int16))
+
+
 @pytest.mark.parametrize("shape", [
     # (B, H, N, d, dv, topk, causal)
     (1, 2, 300, 128, 128, 16, False),
