@@ -753,46 +753,82 @@ cudaError_t launch_bwd_dv(const BwdTcParams& p, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------- small kernels
-// One warp per padded query row: stats[bh][tile][plane][r].  Lane l reads
-// d_v / 32 consecutive values of dO (bf16) and out (fp32) in one vector load each.
+// Four padded query rows per warp: stats[bh][tile][plane][r].  Lane l reads
+// d_v / 32 consecutive values of dO (bf16) and out (fp32) of each row in one
+// vector load each, and every load of the four rows is issued before the first
+// sum, so that a warp keeps about 3 KB in flight.  The four rows (a multiple
+// of four within one 128-row tile) share (bh, tile).
+constexpr int kStatsRowsPerWarp = 4;
 template <int DV>
 __global__ void __launch_bounds__(256)
     bwd_stats_kernel(const __nv_bfloat16* __restrict__ dO, const float* __restrict__ out,
                      const float* __restrict__ lse, const float* __restrict__ qmul,
                      float* __restrict__ stats, int BH, int N, int NT, float alpha) {
   constexpr int E = DV / 32;  // 2 or 4
-  const long long R = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  constexpr int RW = kStatsRowsPerWarp;
+  const long long R0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RW;
   const long long rows = static_cast<long long>(BH) * NT * kTileRows;
-  if (R >= rows) return;
+  if (R0 >= rows) return;
   const int lane = threadIdx.x & 31;
-  const int bh = static_cast<int>(R / (static_cast<long long>(NT) * kTileRows));
-  const int i = static_cast<int>(R % (static_cast<long long>(NT) * kTileRows));
-  float qm = 0.f, nl = -INFINITY, dn = 0.f;
-  if (i < N) {
-    const size_t off = (static_cast<size_t>(bh) * N + i) * DV + lane * E;
-    float acc = 0.f;
-    if constexpr (E == 4) {
-      const uint2 g = __ldg(reinterpret_cast<const uint2*>(dO + off));
-      const float4 o = __ldg(reinterpret_cast<const float4*>(out + off));
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
-      acc = fmaf(a.x, o.x, fmaf(a.y, o.y, fmaf(b.x, o.z, b.y * o.w)));
-    } else {
-      const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(dO + off));
-      const float2 o = __ldg(reinterpret_cast<const float2*>(out + off));
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
-      acc = fmaf(a.x, o.x, a.y * o.y);
-    }
+  const int bh = static_cast<int>(R0 / (static_cast<long long>(NT) * kTileRows));
+  const int i0 = static_cast<int>(R0 % (static_cast<long long>(NT) * kTileRows));
+  float a[RW][E], o[RW][E], qm[RW], lr[RW];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    qm = qmul[R];
-    nl = -lse[static_cast<size_t>(bh) * N + i] * 1.4426950408889634f;
-    dn = -acc * alpha;
+  for (int r = 0; r < RW; ++r) {
+    const int i = i0 + r;
+#pragma unroll
+    for (int e = 0; e < E; ++e) a[r][e] = o[r][e] = 0.f;
+    qm[r] = 0.f;
+    lr[r] = INFINITY;
+    if (i < N) {
+      const size_t off = (static_cast<size_t>(bh) * N + i) * DV + lane * E;
+      if constexpr (E == 4) {
+        const uint2 g = __ldg(reinterpret_cast<const uint2*>(dO + off));
+        const float4 v = __ldg(reinterpret_cast<const float4*>(out + off));
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+        a[r][0] = x.x; a[r][1] = x.y; a[r][2] = y.x; a[r][3] = y.y;
+        o[r][0] = v.x; o[r][1] = v.y; o[r][2] = v.z; o[r][3] = v.w;
+      } else {
+        const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(dO + off));
+        const float2 v = __ldg(reinterpret_cast<const float2*>(out + off));
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
+        a[r][0] = x.x; a[r][1] = x.y;
+        o[r][0] = v.x; o[r][1] = v.y;
+      }
+      qm[r] = __ldg(qmul + R0 + r);
+      lr[r] = __ldg(lse + static_cast<size_t>(bh) * N + i);
+    }
   }
-  if (lane < 4) {
+  float acc[RW];
+#pragma unroll
+  for (int r = 0; r < RW; ++r) {
+    float t = 0.f;
+#pragma unroll
+    for (int e = E - 1; e >= 0; --e) t = fmaf(a[r][e], o[r][e], t);
+    acc[r] = t;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int r = 0; r < RW; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+  // lane 4p + r writes plane p of row r (planes: multiplier, -lse log2 e, -D/sqrt(m), 0)
+  if (lane < 4 * RW) {
+    const int p = lane / RW, r = lane % RW, i = i0 + r;
+    float q = qm[0], l = lr[0], s = acc[0];  // row r's values, without indexing by lane
+#pragma unroll
+    for (int j = 1; j < RW; ++j)
+      if (r == j) {
+        q = qm[j];
+        l = lr[j];
+        s = acc[j];
+      }
+    float v = 0.f;
+    if (p == 0) v = q;
+    else if (p == 1) v = i < N ? -l * 1.4426950408889634f : -INFINITY;
+    else if (p == 2) v = i < N ? -s * alpha : 0.f;
     const size_t base = ((static_cast<size_t>(bh) * NT + i / kTileRows) * 4) * kTileRows + i % kTileRows;
-    const float v = lane == 0 ? qm : lane == 1 ? nl : lane == 2 ? dn : 0.f;
-    stats[base + static_cast<size_t>(lane) * kTileRows] = v;
+    stats[base + static_cast<size_t>(p) * kTileRows] = v;
   }
 }
 
@@ -854,10 +890,10 @@ cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const fl
   const long long rows = static_cast<long long>(BH) * NT * kTileRows;
   if (rows == 0) return cudaSuccess;
   if (dv == 128)
-    bwd_stats_kernel<128><<<blocks_for(rows, 8), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
+    bwd_stats_kernel<128><<<blocks_for(rows, 8 * kStatsRowsPerWarp), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
                                                                    NT, alpha);
   else if (dv == 64)
-    bwd_stats_kernel<64><<<blocks_for(rows, 8), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
+    bwd_stats_kernel<64><<<blocks_for(rows, 8 * kStatsRowsPerWarp), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
                                                                   NT, alpha);
   else
     return cudaErrorInvalidValue;
