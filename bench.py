@@ -96,20 +96,26 @@ def load_peaks():
         return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
 
 
-def kernel_source_hash() -> str:
-    h = hashlib.sha256()
-    for rel in ("projected_feature_efficient_gb300/csrc/attn_ws.cu",
+ATTN_SOURCES = ("projected_feature_efficient_gb300/csrc/attn_ws.cu",
                 "projected_feature_efficient_gb300/csrc/ptx.cuh",
-                "projected_feature_efficient_gb300/csrc/waits.cuh"):
+                "projected_feature_efficient_gb300/csrc/waits.cuh")
+TOPK_SOURCES = ("projected_feature_efficient_gb300/csrc/topk.cu",)
+
+
+def kernel_source_hash(sources=ATTN_SOURCES) -> str:
+    h = hashlib.sha256()
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"attn_ws_{workload}_dram.md")
+def recorded_traffic(workload: str = None, profile: str = None, sources=ATTN_SOURCES):
+    """DRAM bytes per launch from a committed ncu summary (the attention
+    kernel's for `workload` by default), if it was taken on the current kernel
+    source; else None."""
+    name = profile or f"attn_ws_{workload}_dram.md"
+    path = os.path.join(ROOT, "profiles", name)
     try:
         vals = {}
         with open(path) as f:
@@ -117,7 +123,7 @@ def recorded_traffic(workload: str):
                 if ":" in line and line.startswith("- "):
                     k, v = line[2:].split(":", 1)
                     vals[k.strip()] = v.strip().strip("`")
-        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash(sources):
             return None
         return float(vals["dram_bytes_per_full_launch"])
     except Exception:
@@ -807,7 +813,9 @@ def run_sfa(args, rank, world, local_rank):
                        "api": "spa_sfa_attention_fwd", "l2": "inputs (805 MB) exceed L2",
                        "parallelism": f"dp{world}"},
             "roofline": {"bound": "hbm", "achieved": tk_gbs, "peak": hbm[0], "unit": "GB/s",
-                         "frac": tk_gbs / hbm[0], "traffic": None,
+                         "frac": tk_gbs / hbm[0],
+                         "traffic": (recorded_traffic(profile="topk_rows_bf16_sfa_C4.md",
+                                                      sources=TOPK_SOURCES) if H == 32 else None),
                          "kernel": "topk_rows_bf16_kernel (reads and writes q: 2 x 2 bytes per value)",
                          "peak_source": hbm[1]},
             "kernels_ms_per_step": {"topk_q": tk_ms, "rest": t_ms / K - tk_ms},
