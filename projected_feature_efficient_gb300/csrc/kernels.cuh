@@ -129,6 +129,22 @@ cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, in
 cudaError_t launch_bwd_dup_p(const __nv_bfloat16* P, uint16_t* P2, int H, int d, int m,
                              cudaStream_t stream);
 cudaError_t launch_bwd_fold(const float* R, float* dP, int H, int d, int m, cudaStream_t stream);
+// The projection gradients in one pass on the tensor cores (m = 32, d = 128):
+// dq = dQp [P_h; P_h]^T-style products of the bf16 hi | lo split, dk likewise,
+// dP_h accumulated per head in tensor memory and bulk-added into dP.
+struct BwdFinishParams {
+  CUtensorMap qmap, kmap;    // q, k as 3-D (d, N, BH), bf16, 128-byte swizzle, box (64,128,1)
+  CUtensorMap xkmap;         // dKp rows [BH][N][2m] bf16 hi | lo, same encoding (2m = 64)
+  CUtensorMap dqmap, dkmap;  // dq, dk fp32 (d, N, BH), 128-byte swizzle, box (32,128,1)
+  const float* dqacc;        // [BH][NT][128*m] fp32 dQp accumulator (swizzled rows)
+  const __nv_bfloat16* P;    // [H][d][m]
+  float* dP;                 // [H][d][m] fp32, zeroed before the launch
+  int* err;                  // device error word
+  int B, H, N, NT, d, m;
+  unsigned long long limit_ns;  // time limit of every wait in the kernel
+};
+bool bwd_finish_tc_supported(int d, int m);
+cudaError_t launch_bwd_finish_tc(const BwdFinishParams& p, cudaStream_t stream);
 // dq, dk, dP from the split dQp / dKp rows (library GEMMs on bf16, fp32 accumulation)
 int run_backward_post(const void* q, const void* k, const uint16_t* P2, const uint16_t* xq,
                       const uint16_t* xk, float* R, float* dq, float* dk, float* dP, int B,

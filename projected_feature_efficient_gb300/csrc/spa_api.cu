@@ -470,6 +470,27 @@ int bwd_stage_finish(const void* q, const void* k, const void* P, float* dq, flo
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
   const int BH = B * H;
   int st;
+  if (spa::bwd_finish_tc_supported(d, m)) {  // one tensor-core pass
+    spa::BwdFinishParams fp{};
+    if ((st = encode_bf16_rows(&fp.qmap, q, d, N, BH)) ||
+        (st = encode_bf16_rows(&fp.kmap, k, d, N, BH)) ||
+        (st = encode_bf16_rows(&fp.xkmap, w + L.xk, 2 * m, N, BH)) ||
+        (st = encode_rows_map(&fp.dqmap, dq, d, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
+        (st = encode_rows_map(&fp.dkmap, dk, d, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
+        (st = device_error_ptr(&fp.err)))
+      return st;
+    fp.dqacc = reinterpret_cast<const float*>(w + L.dqacc);
+    fp.P = static_cast<const __nv_bfloat16*>(P);
+    fp.dP = dP;
+    fp.B = B;
+    fp.H = H;
+    fp.N = N;
+    fp.NT = L.fwd.NT;
+    fp.d = d;
+    fp.m = m;
+    fp.limit_ns = kWaitLimitNs;
+    return cuda_status(spa::launch_bwd_finish_tc(fp, stream));
+  }
   uint16_t* xq = reinterpret_cast<uint16_t*>(w + L.xq);
   uint16_t* xk = reinterpret_cast<uint16_t*>(w + L.xk);
   uint16_t* p2 = reinterpret_cast<uint16_t*>(w + L.p2);

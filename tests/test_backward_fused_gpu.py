@@ -80,6 +80,10 @@ FUSED_SHAPES = [
     (2, 1, 129, 96, 16, 64, False),     # d = 96, d_v = 64
     (4, 16, 512, 64, 32, 64, True),     # 256 items: several per CTA
     (2, 40, 256, 64, 16, 128, False),   # 160 items, non-causal order
+    # d = 128, m = 32: the projection gradients in one tensor-core pass
+    (1, 3, 50, 128, 32, 128, True),     # one partial tile per (side, b, h)
+    (3, 5, 700, 128, 32, 64, False),    # dP_h summed over three batch entries, ragged
+    (2, 24, 1024, 128, 32, 128, True),  # 768 units: CTA ranges cross heads
 ]
 
 
