@@ -243,7 +243,9 @@ SPA_API int spa_attention_bwd_lse(const void *q, const void *k, const void *v, c
  *            (D_i = <dO_i, out_i>, lse) and a zeroed dQp accumulator.
  *   apply:   the tensor-core kernel; writes dv and leaves dQp, dKp in the
  *            workspace.
- *   finish:  dq, dk, dP from dQp, dKp (library GEMMs).
+ *   finish:  dq, dk, dP from dQp, dKp: one tensor-core pass for d = 128 and
+ *            m = 32 (dP is summed with floating-point reduce-adds whose order
+ *            may vary), library GEMMs otherwise.
  * prepare + apply + finish gives exactly spa_attention_bwd_lse.
  */
 SPA_API int spa_attention_bwd_workspace_size(int B, int H, int N, int d, int m, int d_v,
