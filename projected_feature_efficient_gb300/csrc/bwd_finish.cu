@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
+#include "bwd_common.cuh"
 #include "ptx.cuh"
 
 namespace spa {
@@ -59,19 +60,6 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t a, uint32_t (&v)[4]) {
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
                : "r"(a));
-}
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   gdst),
-               "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-// bf16 hi | lo of two values: hi = bf16(v), lo = bf16(v - hi)
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-  hi = static_cast<uint32_t>(__bfloat16_as_ushort(ha)) |
-       (static_cast<uint32_t>(__bfloat16_as_ushort(hb)) << 16);
-  lo = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
 }
 
 struct Unit {
@@ -207,7 +195,7 @@ __global__ void __launch_bounds__(kFinThreads) bwd_finish_kernel(
       uint32_t hi[16], lo[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        split2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), hi[j], lo[j]);
+        split_pair(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), hi[j], lo[j]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         st_shared_v4(row + ((c ^ sw) << 4), hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);

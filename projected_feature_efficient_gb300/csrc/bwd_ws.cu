@@ -58,6 +58,7 @@
 #include <math.h>
 
 #include "kernels.cuh"
+#include "bwd_common.cuh"
 #include "ptx.cuh"
 #include "waits.cuh"
 
@@ -151,21 +152,7 @@ __device__ __forceinline__ BItem bwd_item(const BwdTcParams& p, int w) {
   return it;
 }
 
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   gdst),
-               "r"(ssrc), "r"(bytes)
-               : "memory");
-}
 
-// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): two values at a time as
-// bf16 pairs (16 significant bits of each value)
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-  hi = static_cast<uint32_t>(__bfloat16_as_ushort(ha)) |
-       (static_cast<uint32_t>(__bfloat16_as_ushort(hb)) << 16);
-  lo = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
-}
 
 __device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) {
   lo = __uint_as_float(v << 16);
