@@ -393,10 +393,14 @@ BwdLayout make_bwd_layout(int B, int H, int N, int d, int m, int dv, bool own_ls
   L.kb = take(rows * m * 2);
   L.stats = take(rows * 4 * sizeof(float));
   L.dqacc = take(rows * m * sizeof(float));
-  L.xq = take(BH * N * 2 * m * 2);
   L.xk = take(BH * N * 2 * m * 2);
-  L.p2 = take(static_cast<size_t>(H) * d * 2 * m * 2);
-  L.R = take(static_cast<size_t>(H) * d * 2 * m * sizeof(float));
+  // the library-GEMM finish also needs the split dQp rows, [P_h | P_h] and the
+  // dP partials; the one-pass finish reads dQp and P_h as they are
+  if (!spa::bwd_finish_tc_supported(d, m)) {
+    L.xq = take(BH * N * 2 * m * 2);
+    L.p2 = take(static_cast<size_t>(H) * d * 2 * m * 2);
+    L.R = take(static_cast<size_t>(H) * d * 2 * m * sizeof(float));
+  }
   if (own_lse) {
     L.lse = take(BH * N * sizeof(float));
     L.out2 = take(BH * N * dv * sizeof(float));
