@@ -79,6 +79,12 @@ struct TopkParams {
   long long rows;
   int d, k;       // d in {32, 64, 128, 256}, 1 <= k <= d
   int bf16;       // element type: 1 = bf16, 0 = fp32
+  // bf16 rows of 64 or 128 features through TMA (when use_tma): x and y as
+  // 3-D (d, rows, 1) bf16 maps, 128-byte swizzle, box (64, 128, 1)
+  int use_tma;
+  CUtensorMap xmap, ymap;
+  int* err;       // device error word (a bounded wait that ran out)
+  unsigned long long limit_ns;
 };
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream);  // P[h] = I_d

@@ -854,6 +854,16 @@ int spa_topk_features(const void* x, void* y, long long rows, int d, int k, int 
   tp.d = d;
   tp.k = k;
   tp.bf16 = dtype == SPA_BF16;
+  // bf16 rows of 64 or 128 features go through TMA (row coordinates are 32-bit)
+  if (tp.bf16 && (d == 64 || d == 128) && rows <= 0x7fffff00LL) {
+    int st;
+    if ((st = encode_bf16_rows(&tp.xmap, x, d, static_cast<int>(rows), 1)) ||
+        (st = encode_bf16_rows(&tp.ymap, y, d, static_cast<int>(rows), 1)) ||
+        (st = device_error_ptr(&tp.err)))
+      return st;
+    tp.use_tma = 1;
+    tp.limit_ns = kWaitLimitNs;
+  }
   return cuda_status(spa::launch_topk(tp, static_cast<cudaStream_t>(stream)));
 }
 

@@ -17,6 +17,7 @@
 #include <stdint.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace spa {
 namespace {
@@ -277,6 +278,109 @@ __global__ void __launch_bounds__(128) topk_rows_bf16_kernel(const uint16_t* __r
   for (int q = tid; q < nrows * V; q += 128) dst[q] = tile[slot(q / V, q % V)];
 }
 
+// bf16 rows of 64 or 128 features, persistent: a CTA walks blocks of 128 rows
+// (blockIdx.x, + gridDim.x, ...) through two shared-memory buffers.  One
+// thread brings a block in by TMA (64-feature boxes, 128-byte swizzle: chunk
+// c of row r at chunk c ^ (r % 8) of its box row, so the per-row reads of a
+// quarter warp hit eight bank groups) two blocks ahead; every thread selects
+// its row (select_row) and writes the kept values back over the same slots;
+// the block leaves by TMA stores (rows past the end are clipped), and the
+// buffer is refilled once those stores have read it.  Bounded waits: a wait
+// that runs out sets the device error word, and the CTA lets its own copies
+// land before it exits.
+template <int D>
+__global__ void __launch_bounds__(128) topk_rows_bf16_tma_kernel(
+    const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+    long long nblocks, int k, int* err, unsigned long long limit_ns) {
+  using namespace ptx;
+  constexpr int G = D / 32, V = D / 8, NB = D / 64;  // groups, 16-byte chunks, boxes per row
+  constexpr int kBox = 128 * 128;                    // one box: 128 rows x 128 bytes
+  constexpr int kBuf = NB * kBox;                    // one block of 128 rows
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[2];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sptr = smem_raw + (sbase - smem_u32(smem_raw));
+  const int tid = threadIdx.x;
+  const long long step = gridDim.x;
+  int issued0 = 0, issued1 = 0;  // thread 0: loads started into buffer 0 / 1
+  auto load = [&](long long blk, int s) {
+    mbar_arrive_expect_tx(&full[s], kBuf);
+#pragma unroll
+    for (int h = 0; h < NB; ++h)
+      tma_load_3d(sptr + s * kBuf + h * kBox, &xmap, h * 64, static_cast<int>(blk * 128), 0,
+                  &full[s]);
+    if (s == 0) ++issued0;
+    else ++issued1;
+  };
+  if (tid == 0) {
+    prefetch_tmap(&xmap);
+    prefetch_tmap(&ymap);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const long long b0 = blockIdx.x;
+  if (tid == 0) {
+    if (b0 < nblocks) load(b0, 0);
+    if (b0 + step < nblocks) load(b0 + step, 1);
+  }
+  const uint32_t sw = static_cast<uint32_t>(tid & 7);
+  bool ok = true;
+  int i = 0;
+  for (long long b = b0; b < nblocks; b += step, ++i) {
+    const int s = i & 1;
+    ok = __syncthreads_and(mbar_wait(&full[s], (i >> 1) & 1, limit_ns));
+    if (!ok) break;
+    const uint32_t row = sbase + s * kBuf + tid * 128;  // this thread's row in box 0
+    uint32_t a[G][16];
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      uint32_t t[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(t[0]), "=r"(t[1]), "=r"(t[2]), "=r"(t[3])
+                   : "r"(row + (c / 8) * kBox + (((c % 8) ^ sw) << 4)));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[c / 4][(c % 4) * 4 + e] = t[e];
+    }
+    uint32_t keep[G];
+    select_row<G>(a, k, keep);
+    // read the row again rather than keep it in registers through the search
+    asm volatile("" ::: "memory");
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      const uint32_t addr = row + (c / 8) * kBox + (((c % 8) ^ sw) << 4);
+      uint32_t t[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(t[0]), "=r"(t[1]), "=r"(t[2]), "=r"(t[3])
+                   : "r"(addr));
+      const int g = c / 4, w = (c % 4) * 4;
+      st_shared_v4(addr, kept_word<G>(t[0], keep, g, w), kept_word<G>(t[1], keep, g, w + 1),
+                   kept_word<G>(t[2], keep, g, w + 2), kept_word<G>(t[3], keep, g, w + 3));
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int h = 0; h < NB; ++h)
+        tma_store_3d(&ymap, sbase + s * kBuf + h * kBox, h * 64, static_cast<int>(b * 128), 0);
+      bulk_commit_group();
+      if (b + 2 * step < nblocks) {
+        bulk_wait_group_read<0>();  // the stores have read this buffer
+        load(b + 2 * step, s);
+      }
+    }
+  }
+  if (tid == 0) {
+    if (!ok) atomicExch(err, 1);
+    // loads started and not consumed land before the CTA's memory is released
+    // (i iterations ran to completion: (i + 1) / 2 of them used buffer 0, i / 2 buffer 1)
+    if (issued0 > (i + 1) / 2) mbar_wait(&full[0], (issued0 - 1) & 1, limit_ns);
+    if (issued1 > i / 2) mbar_wait(&full[1], (issued1 - 1) & 1, limit_ns);
+    bulk_wait_group_read<0>();
+  }
+}
+
 template <typename T>
 cudaError_t launch_typed(const TopkParams& p, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>((p.rows + 7) / 8);
@@ -316,7 +420,7 @@ cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream
 }
 
 template <int D>
-cudaError_t launch_bf16_rows(const TopkParams& p, cudaStream_t stream) {
+cudaError_t launch_bf16_rows_staged(const TopkParams& p, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>((p.rows + 127) / 128);
   const uint16_t* x = static_cast<const uint16_t*>(p.x);
   uint16_t* y = static_cast<uint16_t*>(p.y);
@@ -327,14 +431,36 @@ cudaError_t launch_bf16_rows(const TopkParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_bf16_rows_tma(const TopkParams& p, cudaStream_t stream) {
+  constexpr int kSmem = 2 * (D / 64) * 128 * 128 + 1024;
+  auto kern = topk_rows_bf16_tma_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, kSmem)) !=
+      cudaSuccess)
+    return e;
+  const long long nblocks = (p.rows + 127) / 128;
+  const long long cap = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+  const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
+  kern<<<grid, 128, kSmem, stream>>>(p.xmap, p.ymap, nblocks, p.k, p.err, p.limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
   if (p.rows > 8LL * 0x7fffffffLL) return cudaErrorInvalidValue;
   // bf16 rows up to 128 features: a thread per row (16-byte row accesses; x
   // and y are 16-byte aligned and every row is a multiple of 16 bytes)
-  if (p.bf16 && p.d == 128) return launch_bf16_rows<128>(p, stream);
-  if (p.bf16 && p.d == 64) return launch_bf16_rows<64>(p, stream);
-  if (p.bf16 && p.d == 32) return launch_bf16_rows<32>(p, stream);
+  if (p.bf16 && p.use_tma && p.d == 128) return launch_bf16_rows_tma<128>(p, stream);
+  if (p.bf16 && p.use_tma && p.d == 64) return launch_bf16_rows_tma<64>(p, stream);
+  if (p.bf16 && p.d == 128) return launch_bf16_rows_staged<128>(p, stream);
+  if (p.bf16 && p.d == 64) return launch_bf16_rows_staged<64>(p, stream);
+  if (p.bf16 && p.d == 32) return launch_bf16_rows_staged<32>(p, stream);
   return p.bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);
 }
 

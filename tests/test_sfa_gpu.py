@@ -50,6 +50,19 @@ def test_topk_full_size_sampled():
     assert torch.equal(got[idx].view(torch.int16), want.view(torch.int16))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_topk_in_place_matches(d):
+    """Writing the sparsified rows over the input gives the same bits as a
+    separate output (each block of rows is read before it is written)."""
+    pkg = spa()
+    x = rows_with_ties(70_000, d, torch.bfloat16, seed=3 + d).cuda()
+    want = pkg.spa_topk_features(x, 9)
+    y = x.clone()
+    got = pkg.spa_topk_features(y, 9, out=y)
+    assert got.data_ptr() == y.data_ptr()
+    assert torch.equal(y.view(torch.int16), want.view(torch.int16))
+
+
 @pytest.mark.parametrize("shape", [
     # (B, H, N, d, dv, topk, causal)
     (1, 2, 300, 128, 128, 16, False),
