@@ -816,7 +816,7 @@ def run_sfa(args, rank, world, local_rank):
                          "frac": tk_gbs / hbm[0],
                          "traffic": (recorded_traffic(profile="topk_rows_bf16_sfa_C4.md",
                                                       sources=TOPK_SOURCES) if H == 32 else None),
-                         "kernel": "topk_rows_bf16_kernel (reads and writes q: 2 x 2 bytes per value)",
+                         "kernel": "topk_rows_bf16_tma_kernel (reads and writes q: 2 x 2 bytes per value)",
                          "peak_source": hbm[1]},
             "kernels_ms_per_step": {"topk_q": tk_ms, "rest": t_ms / K - tk_ms},
             "gpu_launches": 5 * K,  # Top-k of q and k, P = I, projection, attention
