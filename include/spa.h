@@ -140,10 +140,10 @@ SPA_API int spa_attention_apply(const void *v, float *out, int B, int H, int N, 
  * to the device, runs the forward, copies out back, and synchronises `stream`
  * before returning, so `out` is valid on return.  Heads are independent, so
  * the (batch, head) range is cut into chunks of whole heads (at least about
- * 32 MB of traffic each, at most 16 chunks) that run on three internal
- * streams forked from and joined back into `stream`: chunk c+1 is copied in
- * and chunk c-1 copied out while chunk c computes.  The result is bit for bit
- * that of spa_attention_fwd.  Device buffers and workspace for three chunks
+ * 32 MB of traffic each, at most 32 chunks) that run on four internal
+ * streams forked from and joined back into `stream`: later chunks are copied
+ * in and earlier ones copied out while a chunk computes.  The result is bit for
+ * bit that of spa_attention_fwd.  Device buffers and workspace for four chunks
  * are taken on `stream` from a memory pool the library keeps per device and
  * released to it before return; the pool holds on to what it has reserved, so
  * that later calls do not reserve device memory again (spa_host_pool_trim
