@@ -141,7 +141,9 @@ SPA_API int spa_attention_apply(const void *v, float *out, int B, int H, int N, 
  * before returning, so `out` is valid on return.  Heads are independent, so
  * the (batch, head) range is cut into chunks of whole heads (at least about
  * 32 MB of traffic each, at most 32 chunks) that run on four internal
- * streams forked from and joined back into `stream`: later chunks are copied
+ * streams (created by the first call on a device and kept until the process
+ * exits; concurrent calls share them) forked from and joined back into
+ * `stream`: later chunks are copied
  * in and earlier ones copied out while a chunk computes.  The result is bit for
  * bit that of spa_attention_fwd.  Device buffers and workspace for four chunks
  * are taken on `stream` from a memory pool the library keeps per device and
