@@ -158,9 +158,9 @@ SPA_API int spa_attention_fwd_host(const void *q, const void *k, const void *v, 
                                    float *out, int B, int H, int N, int d, int m, int d_v,
                                    int causal, int dtype, void *stream);
 
-/* spa_host_pool_trim -- releases the current device's unused staging memory
- * kept by spa_attention_fwd_host (call when no host-buffer forward is running
- * on that device). */
+/* spa_host_pool_trim -- releases the current device's unused memory kept by
+ * the library's pool (the staging of spa_attention_fwd_host and the scratch of
+ * spa_attention_decode; call when neither is running on that device). */
 SPA_API int spa_host_pool_trim(void);
 
 /*
@@ -288,8 +288,11 @@ SPA_API int spa_attention_bwd_finish(const void *q, const void *k, const void *P
  *   q [B][H][d] bf16 and q~ = q P_h in fp32.  Scores, probabilities and P V are
  *   fp32.  The keys are split into chunks processed in parallel and merged by a
  *   log-sum-exp combine; the chunk results (B*H*chunks*(2+d_v) floats) and
- *   q~ (B*H*m floats) are taken with cudaMallocAsync on `stream` and released.  Equivalent to the
- *   last row of the causal forward over the same L keys.
+ *   q~ (B*H*m floats) are taken on `stream` from the memory pool the library
+ *   keeps per device (the one spa_attention_fwd_host uses, which keeps its
+ *   reservation across synchronisations; spa_host_pool_trim releases it) and
+ *   given back to it before return.  Equivalent to the last row of the causal
+ *   forward over the same L keys.
  */
 SPA_API int spa_kcache_append(const void *k, const void *P, void *kc, float *kc_mul, int B, int H,
                               int T, int d, int m, int pos, int cap, int dtype, void *stream);
