@@ -20,8 +20,12 @@
  *              Outputs are always fp32.
  *   Memory     unless an entry point says otherwise, every pointer is a CUDA
  *              device pointer on the current device, 16-byte aligned.  The
- *              caller owns every buffer; the library keeps no device memory
- *              between calls.
+ *              caller owns every buffer it passes.  Between calls the library
+ *              keeps, per device: a memory pool for the workspaces it takes
+ *              itself (what it has reserved stays reserved until
+ *              spa_host_pool_trim), the device error word, the internal
+ *              streams of spa_attention_fwd_host, a library GEMM handle, and
+ *              the fixed scratch array of spa_attention_fwd_noalloc.
  *   stream     a cudaStream_t passed as void* (NULL = legacy default stream).
  *              Work is enqueued asynchronously; the return value reports
  *              argument errors and launch errors only.  Faults inside a kernel
@@ -92,9 +96,11 @@ SPA_API int spa_project(const void *x, const void *P, float *x_proj, int B, int 
  *   SPA_BF16: 1 <= d <= 256; m in {16, 32, 64, 128}; d_v in {64, 128}.
  *   SPA_F32 : 1 <= d <= 256; 1 <= m <= 128;          1 <= d_v <= 256.
  *   N up to 2^31 - 1, B*H up to 65535.
- * A workspace of spa_attention_workspace_size() bytes is taken with
- * cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
- * stream (SPA_ERR_NOMEM if the allocation fails).
+ * A workspace of spa_attention_workspace_size() bytes is taken on `stream`
+ * from the memory pool the library keeps per device and given back to it on
+ * the same stream (SPA_ERR_NOMEM if the allocation fails).  The pool keeps its
+ * reservation across synchronisations, so a synchronised loop of calls does
+ * not reserve device memory again; spa_host_pool_trim releases it.
  */
 SPA_API int spa_attention_fwd(const void *q, const void *k, const void *v, const void *P,
                               float *out, int B, int H, int N, int d, int m, int d_v, int causal,
@@ -159,8 +165,9 @@ SPA_API int spa_attention_fwd_host(const void *q, const void *k, const void *v, 
                                    int causal, int dtype, void *stream);
 
 /* spa_host_pool_trim -- releases the current device's unused memory kept by
- * the library's pool (the staging of spa_attention_fwd_host and the scratch of
- * spa_attention_decode; call when neither is running on that device). */
+ * the library's pool (the workspaces of the allocating entry points, the
+ * staging of spa_attention_fwd_host, the scratch of spa_attention_decode; call
+ * when none of them is running on that device). */
 SPA_API int spa_host_pool_trim(void);
 
 /*
@@ -220,8 +227,9 @@ SPA_API int spa_attention_fwd_lse(const void *q, const void *k, const void *v, c
  *     a time (2 N^2 floats per head), plain cuBLAS products (fp32
  *     accumulation; TF32 products for bf16 inputs, exact for their values;
  *     fp32 products for fp32 inputs).
- * Workspace from cudaMallocAsync on `stream`.  An empty problem (B*H*N == 0)
- * zeroes dP.
+ * Workspace on `stream`: the fused version's from the library's pool (as for
+ * spa_attention_fwd), the materialised version's from cudaMallocAsync.  An
+ * empty problem (B*H*N == 0) zeroes dP.
  */
 SPA_API int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P,
                               const float *out, const void *dO, float *dq, float *dk, float *dv,
@@ -317,7 +325,7 @@ SPA_API int spa_attention_decode(const void *q, const void *P, const void *kc, c
  *   q, k sparsified to topk features per row, i.e. spa_attention_fwd of
  *   (Topk(q), Topk(k), v) with P_h = I_d (m = d, scale 1/sqrt(d)).  d in
  *   {32, 64, 128}.  The sparsified copies, the identity P and the workspace
- *   are taken with cudaMallocAsync on `stream` and released.
+ *   are taken on `stream` from the library's pool and given back to it.
  */
 SPA_API int spa_topk_features(const void *x, void *y, long long rows, int d, int k, int dtype,
                               void *stream);

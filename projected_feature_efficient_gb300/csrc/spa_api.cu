@@ -289,6 +289,21 @@ int host_pool(cudaMemPool_t* out) {
   *out = g_host_pool[dev];
   return SPA_OK;
 }
+// Stream-ordered workspace from the library's pool: it keeps what it has
+// reserved across synchronisations, so calls in a synchronised loop do not
+// reserve device memory again (with the default pool, which hands memory back
+// at every synchronisation, the allocating forward took 0.64 ms per call on C3
+// against 0.36 ms on a caller workspace).  Released with cudaFreeAsync.
+int pool_alloc(void** p, size_t bytes, cudaStream_t s) {
+  cudaMemPool_t pool = nullptr;
+  if (host_pool(&pool) != SPA_OK) return SPA_ERR_CUDA;
+  if (cudaMallocFromPoolAsync(p, bytes, pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  return SPA_OK;
+}
+
 // The host-buffer forward's internal streams, created once per device and kept
 // until the process exits (creating and destroying them took about 0.05 ms of
 // every call).  Calls from several threads may share them: each call orders
@@ -628,10 +643,7 @@ int backward_entry(const void* q, const void* k, const void* v, const void* P, c
     return SPA_ERR_ALIGN;
   const size_t bytes = make_bwd_layout(B, H, N, d, m, d_v, lse == nullptr).total;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
-  }
+  if (int e = pool_alloc(&ws, bytes, s)) return e;
   st = run_backward_fused(q, k, v, P, out, lse, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal,
                           static_cast<char*>(ws), s);
   const cudaError_t fe = cudaFreeAsync(ws, s);
@@ -750,10 +762,7 @@ int spa_attention_fwd(const void* q, const void* k, const void* v, const void* P
   const size_t bytes = make_layout(B, H, N, m, dtype).total;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
-  }
+  if (int e = pool_alloc(&ws, bytes, s)) return e;
   st = run_forward(q, k, v, P, out, B, H, N, d, m, d_v, causal, dtype, ws, s);
   const cudaError_t fe = cudaFreeAsync(ws, s);
   if (st) return st;
@@ -913,10 +922,7 @@ int spa_sfa_attention_fwd(const void* q, const void* k, const void* v, float* ou
   const size_t total = ow + make_layout(B, H, N, d, dtype).total;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* buf = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&buf), total, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
-  }
+  if (int e = pool_alloc(reinterpret_cast<void**>(&buf), total, s)) return e;
   st = spa_topk_features(q, buf + oq, rows, d, topk, dtype, stream);
   if (!st) st = spa_topk_features(k, buf + ok, rows, d, topk, dtype, stream);
   if (!st) st = cuda_status(spa::launch_identity(buf + op, H, d, dtype == SPA_BF16, s));
@@ -959,10 +965,7 @@ int spa_attention_fwd_lse(const void* q, const void* k, const void* v, const voi
   const size_t bytes = make_layout(B, H, N, m, dtype).total;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
-  }
+  if (int e = pool_alloc(&ws, bytes, s)) return e;
   st = run_prepare(q, k, P, B, H, N, d, m, dtype, ws, s);
   if (!st) st = run_apply(v, out, B, H, N, m, d_v, causal, dtype, ws, s, kWaitLimitNs, 0, lse);
   const cudaError_t fe = cudaFreeAsync(ws, s);
