@@ -18,6 +18,7 @@ __all__ = [
     "spa_attention_decode", "spa_topk_features", "spa_sfa_attention_fwd", "spa_attention_bwd",
     "spa_attention_fwd_lse", "spa_attention_bwd_lse", "spa_attention_bwd_workspace_size",
     "spa_attention_bwd_prepare", "spa_attention_bwd_apply", "spa_attention_bwd_finish",
+    "host_pool_trim",
 ]
 
 

@@ -368,3 +368,8 @@ def device_error() -> int:
     c = _i(0)
     _check(lib.spa_device_error(ctypes.byref(c)), "spa_device_error")
     return int(c.value)
+
+
+def host_pool_trim() -> None:
+    """Release the current device's unused memory kept by the library's pool."""
+    _check(lib.spa_host_pool_trim(), "spa_host_pool_trim")
