@@ -740,82 +740,103 @@ cudaError_t launch_bwd_dv(const BwdTcParams& p, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------- small kernels
-// Four padded query rows per warp: stats[bh][tile][plane][r].  Lane l reads
-// d_v / 32 consecutive values of dO (bf16) and out (fp32) of each row in one
-// vector load each, and every load of the four rows is issued before the first
-// sum, so that a warp keeps about 3 KB in flight.  The four rows (a multiple
-// of four within one 128-row tile) share (bh, tile).
-constexpr int kStatsRowsPerWarp = 4;
+// Row statistics of the backward, stats[bh][tile][plane][r] with the planes
+// (Q row multiplier, -lse log2 e, -D_i / sqrt(m), 0), D_i = <dO_i, out_i>.
+// Persistent: a CTA walks (bh, 128-row tile) blocks,
+// each brought in by TMA two blocks ahead through two buffers (dO as
+// 64-column bf16 boxes, out as 32-column fp32 boxes, 128-byte swizzle, rows
+// past N zero-filled); thread r sums row r's <dO, out> from shared memory (16-
+// byte chunk c of a box row at c ^ (r % 8): a quarter warp's reads hit eight
+// bank groups) and writes the tile's four statistics planes coalesced.
 template <int DV>
-__global__ void __launch_bounds__(256)
-    bwd_stats_kernel(const __nv_bfloat16* __restrict__ dO, const float* __restrict__ out,
-                     const float* __restrict__ lse, const float* __restrict__ qmul,
-                     float* __restrict__ stats, int BH, int N, int NT, float alpha) {
-  constexpr int E = DV / 32;  // 2 or 4
-  constexpr int RW = kStatsRowsPerWarp;
-  const long long R0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RW;
-  const long long rows = static_cast<long long>(BH) * NT * kTileRows;
-  if (R0 >= rows) return;
-  const int lane = threadIdx.x & 31;
-  const int bh = static_cast<int>(R0 / (static_cast<long long>(NT) * kTileRows));
-  const int i0 = static_cast<int>(R0 % (static_cast<long long>(NT) * kTileRows));
-  float a[RW][E], o[RW][E], qm[RW], lr[RW];
+__global__ void __launch_bounds__(128) bwd_stats_tma_kernel(
+    const __grid_constant__ CUtensorMap domap, const __grid_constant__ CUtensorMap omap,
+    const float* __restrict__ lse, const float* __restrict__ qmul, float* __restrict__ stats,
+    int BH, int N, int NT, float alpha, int* err, unsigned long long limit_ns) {
+  constexpr int kBox = 128 * 128;              // one 128-row x 128-byte box
+  constexpr int kDoBoxes = DV / 64, kOBoxes = DV / 32;
+  constexpr int kBuf = (kDoBoxes + kOBoxes) * kBox;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[2];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sptr = smem_raw + (sbase - smem_u32(smem_raw));
+  const int tid = threadIdx.x;
+  const long long nblocks = static_cast<long long>(BH) * NT, step = gridDim.x;
+  int issued0 = 0, issued1 = 0;  // thread 0: loads started into buffer 0 / 1
+  auto load = [&](long long blk, int s) {
+    const int bh = static_cast<int>(blk / NT), row0 = static_cast<int>(blk % NT) * kTileRows;
+    mbar_arrive_expect_tx(&full[s], kBuf);
 #pragma unroll
-  for (int r = 0; r < RW; ++r) {
-    const int i = i0 + r;
+    for (int h = 0; h < kDoBoxes; ++h)
+      tma_load_3d(sptr + s * kBuf + h * kBox, &domap, h * 64, row0, bh, &full[s]);
 #pragma unroll
-    for (int e = 0; e < E; ++e) a[r][e] = o[r][e] = 0.f;
-    qm[r] = 0.f;
-    lr[r] = INFINITY;
-    if (i < N) {
-      const size_t off = (static_cast<size_t>(bh) * N + i) * DV + lane * E;
-      if constexpr (E == 4) {
-        const uint2 g = __ldg(reinterpret_cast<const uint2*>(dO + off));
-        const float4 v = __ldg(reinterpret_cast<const float4*>(out + off));
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
-        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
-        a[r][0] = x.x; a[r][1] = x.y; a[r][2] = y.x; a[r][3] = y.y;
-        o[r][0] = v.x; o[r][1] = v.y; o[r][2] = v.z; o[r][3] = v.w;
-      } else {
-        const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(dO + off));
-        const float2 v = __ldg(reinterpret_cast<const float2*>(out + off));
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
-        a[r][0] = x.x; a[r][1] = x.y;
-        o[r][0] = v.x; o[r][1] = v.y;
+    for (int h = 0; h < kOBoxes; ++h)
+      tma_load_3d(sptr + s * kBuf + (kDoBoxes + h) * kBox, &omap, h * 32, row0, bh, &full[s]);
+    if (s == 0) ++issued0;
+    else ++issued1;
+  };
+  if (tid == 0) {
+    prefetch_tmap(&domap);
+    prefetch_tmap(&omap);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const long long b0 = blockIdx.x;
+  if (tid == 0) {
+    if (b0 < nblocks) load(b0, 0);
+    if (b0 + step < nblocks) load(b0 + step, 1);
+  }
+  const uint32_t sw = static_cast<uint32_t>(tid & 7);
+  bool ok = true;
+  int it = 0;
+  for (long long b = b0; b < nblocks; b += step, ++it) {
+    const int s = it & 1;
+    ok = __syncthreads_and(mbar_wait(&full[s], (it >> 1) & 1, limit_ns));
+    if (!ok) break;
+    const int bh = static_cast<int>(b / NT), tile = static_cast<int>(b % NT);
+    const int i = tile * kTileRows + tid;
+    const uint32_t dorow = sbase + s * kBuf + tid * 128;
+    const uint32_t orow = dorow + kDoBoxes * kBox;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < DV / 8; ++c) {  // 8 columns: one dO chunk, two out chunks
+      uint32_t g[4], o0[4], o1[4];
+      const uint32_t cg = (c / 8) * kBox + (((c % 8) ^ sw) << 4);
+      const int c0 = 2 * c, c1 = 2 * c + 1;  // out chunks (4 fp32 each)
+      const uint32_t a0 = (c0 / 8) * kBox + (((c0 % 8) ^ sw) << 4);
+      const uint32_t a1 = (c1 / 8) * kBox + (((c1 % 8) ^ sw) << 4);
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(g[0]), "=r"(g[1]), "=r"(g[2]), "=r"(g[3]) : "r"(dorow + cg));
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(o0[0]), "=r"(o0[1]), "=r"(o0[2]), "=r"(o0[3]) : "r"(orow + a0));
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(o1[0]), "=r"(o1[1]), "=r"(o1[2]), "=r"(o1[3]) : "r"(orow + a1));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float lo, hi;
+        unpack_bf16x2(g[e], lo, hi);
+        const uint32_t* o = e < 2 ? o0 : o1;
+        acc = fmaf(lo, __uint_as_float(o[(2 * e) % 4]), acc);
+        acc = fmaf(hi, __uint_as_float(o[(2 * e + 1) % 4]), acc);
       }
-      qm[r] = __ldg(qmul + R0 + r);
-      lr[r] = __ldg(lse + static_cast<size_t>(bh) * N + i);
     }
+    float* st = stats + (static_cast<size_t>(bh) * NT + tile) * 4 * kTileRows + tid;
+    const bool in = i < N;
+    st[0] = in ? qmul[(static_cast<size_t>(bh) * NT + tile) * kTileRows + tid] : 0.f;
+    st[kTileRows] = in ? -lse[static_cast<size_t>(bh) * N + i] * 1.4426950408889634f : -INFINITY;
+    st[2 * kTileRows] = in ? -acc * alpha : 0.f;
+    st[3 * kTileRows] = 0.f;
+    // every thread has read this buffer: refill it two blocks ahead
+    __syncthreads();
+    if (tid == 0 && b + 2 * step < nblocks) load(b + 2 * step, s);
   }
-  float acc[RW];
-#pragma unroll
-  for (int r = 0; r < RW; ++r) {
-    float t = 0.f;
-#pragma unroll
-    for (int e = E - 1; e >= 0; --e) t = fmaf(a[r][e], o[r][e], t);
-    acc[r] = t;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int r = 0; r < RW; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
-  // lane 4p + r writes plane p of row r (planes: multiplier, -lse log2 e, -D/sqrt(m), 0)
-  if (lane < 4 * RW) {
-    const int p = lane / RW, r = lane % RW, i = i0 + r;
-    float q = qm[0], l = lr[0], s = acc[0];  // row r's values, without indexing by lane
-#pragma unroll
-    for (int j = 1; j < RW; ++j)
-      if (r == j) {
-        q = qm[j];
-        l = lr[j];
-        s = acc[j];
-      }
-    float v = 0.f;
-    if (p == 0) v = q;
-    else if (p == 1) v = i < N ? -l * 1.4426950408889634f : -INFINITY;
-    else if (p == 2) v = i < N ? -s * alpha : 0.f;
-    const size_t base = ((static_cast<size_t>(bh) * NT + i / kTileRows) * 4) * kTileRows + i % kTileRows;
-    stats[base + static_cast<size_t>(p) * kTileRows] = v;
+  if (tid == 0) {
+    if (!ok) atomicExch(err, 1);
+    // (it iterations ran to completion: (it + 1) / 2 of them used buffer 0, it / 2 buffer 1)
+    if (issued0 > (it + 1) / 2) mbar_wait(&full[0], (issued0 - 1) & 1, limit_ns);
+    if (issued1 > it / 2) mbar_wait(&full[1], (issued1 - 1) & 1, limit_ns);
   }
 }
 
@@ -871,20 +892,35 @@ cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const float* lse,
-                             const float* qmul, float* stats, int BH, int N, int NT, int dv,
-                             float alpha, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(BH) * NT * kTileRows;
-  if (rows == 0) return cudaSuccess;
-  if (dv == 128)
-    bwd_stats_kernel<128><<<blocks_for(rows, 8 * kStatsRowsPerWarp), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
-                                                                   NT, alpha);
-  else if (dv == 64)
-    bwd_stats_kernel<64><<<blocks_for(rows, 8 * kStatsRowsPerWarp), 256, 0, stream>>>(dO, out, lse, qmul, stats, BH, N,
-                                                                  NT, alpha);
-  else
-    return cudaErrorInvalidValue;
+template <int DV>
+cudaError_t launch_bwd_stats_tma(const BwdStatsMaps& mp, const float* lse, const float* qmul,
+                                 float* stats, int BH, int N, int NT, float alpha,
+                                 cudaStream_t stream) {
+  constexpr int kSmem = 2 * (DV / 64 + DV / 32) * 128 * 128 + 1024;
+  auto kern = bwd_stats_tma_kernel<DV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, kSmem)) !=
+      cudaSuccess)
+    return e;
+  const long long nblocks = static_cast<long long>(BH) * NT;
+  const long long cap = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+  kern<<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), 128, kSmem, stream>>>(
+      mp.domap, mp.omap, lse, qmul, stats, BH, N, NT, alpha, mp.err, mp.limit_ns);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_stats(const BwdStatsMaps& maps, const float* lse, const float* qmul,
+                             float* stats, int BH, int N, int NT, int dv, float alpha,
+                             cudaStream_t stream) {
+  if (static_cast<long long>(BH) * NT == 0) return cudaSuccess;
+  if (dv == 128) return launch_bwd_stats_tma<128>(maps, lse, qmul, stats, BH, N, NT, alpha, stream);
+  if (dv == 64) return launch_bwd_stats_tma<64>(maps, lse, qmul, stats, BH, N, NT, alpha, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, int NT, int m,

@@ -124,10 +124,17 @@ struct BwdTcParams {
 };
 bool bwd_tc_supported(int m, int dv);
 cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream);
-// stats for the backward: one warp per padded query row
-cudaError_t launch_bwd_stats(const __nv_bfloat16* dO, const float* out, const float* lse,
-                             const float* qmul, float* stats, int BH, int N, int NT, int dv,
-                             float alpha, cudaStream_t stream);
+// Row statistics of the backward (persistent, TMA): dO and out as 3-D
+// (d_v, N, BH) maps with 128-byte swizzle and 128-row boxes (bf16 64 columns,
+// fp32 32 columns).
+struct BwdStatsMaps {
+  CUtensorMap domap, omap;
+  int* err;                     // device error word
+  unsigned long long limit_ns;  // time limit of every wait in the kernel
+};
+cudaError_t launch_bwd_stats(const BwdStatsMaps& maps, const float* lse, const float* qmul,
+                             float* stats, int BH, int N, int NT, int dv, float alpha,
+                             cudaStream_t stream);
 // dQp (swizzled tiles) -> bf16 hi | lo rows [BH][N][2m]
 cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, int NT, int m,
                              cudaStream_t stream);

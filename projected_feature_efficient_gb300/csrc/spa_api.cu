@@ -465,10 +465,15 @@ int bwd_stage_inputs(const float* out, const float* lse, const void* dO, int B, 
                                             sizeof(float),
                                         stream))))
     return st;
+  spa::BwdStatsMaps maps{};
+  if ((st = encode_bf16_rows(&maps.domap, dO, d_v, N, BH)) ||
+      (st = encode_rows_map(&maps.omap, out, d_v, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
+      (st = device_error_ptr(&maps.err)))
+    return st;
+  maps.limit_ns = kWaitLimitNs;
   return cuda_status(spa::launch_bwd_stats(
-      static_cast<const __nv_bfloat16*>(dO), out, lse,
-      reinterpret_cast<const float*>(w + L.fwd.qmul), reinterpret_cast<float*>(w + L.stats), BH, N,
-      NT, d_v, alpha, stream));
+      maps, lse, reinterpret_cast<const float*>(w + L.fwd.qmul),
+      reinterpret_cast<float*>(w + L.stats), BH, N, NT, d_v, alpha, stream));
 }
 
 // Fused backward, stage 2: the tensor-core kernel (dV, dKp, dQp).
