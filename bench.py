@@ -1,23 +1,34 @@
 #!/usr/bin/env python3
 """Throughput of the projected-feature attention forward on GB300.
 
-One step = the whole forward (projection of Q and K, scores, online softmax,
-value product) over one batch of the workload
+One pass = the whole forward (projection of Q and K, scores, online softmax,
+value product) over one batch of a workload, inputs resident in HBM.  The
+default workload is
     C4: B=1, H=32, N=32768, d=128, m=32, d_v=128, bf16, non-causal,
-        Q, K, V iid N(0, 1), P iid N(0, 1/m) per head
-with inputs resident in HBM.  The metric is TFLOP/s with
+        Q, K, V iid N(0, 1), P iid N(0, 1/m) per head;
+--config picks any of the method's workloads (C1 fp32 N=256; C2 N=2048;
+C3 N=8192 causal; C4 N=32768 with --m 16|32|64; C5 N=131072 causal; C5ctl,
+the exact-attention control m=d=128, P=I), and --sweep measures all of them
+(the metric is quoted against N and m), one JSON line each, optionally
+appended to a --results file that a rerun resumes from.  The metric is
+TFLOP/s with
     FLOPs = 4 B H N d m + 2 B H N^2 (m + d_v)     (N^2 term halved if causal)
-and its fraction of the measured bf16 tensor-core peak.
+and its fraction of the measured bf16 tensor-core peak.  A timed step holds
+enough passes (repeats_per_step) that the timed region lasts at least
+--min-seconds; workloads whose inputs fit in L2 get an L2 flush between
+passes, outside the timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config C1|C2|C3|C4|C5|C5ctl] [--m 16|32|64] [--sweep]
     python bench.py --decode     (the decode row: projected key cache, workload D1)
     python bench.py --backward   (the backward row, workload C3)
     python bench.py --sfa        (the Sparse Feature Attention row, C4 shape)
 
-Under torchrun (N > 1) every rank runs the same workload on its own GPU
-(independent problems, no data-path collective: weak scaling); rank 0 prints
-one JSON line.  --impl reference times the fp64 CPU oracle on a bounded sample
-of the same workload on the host cores (rank 0 only).
+Under torchrun (N > 1) the ranks split the B*H independent (batch, head)
+pairs of one problem (shard.shard_pairs; no data-path collective, strong
+scaling); rank 0 prints one JSON line.  --impl reference times the fp64 CPU
+oracle on a bounded sample of the same workload on the host cores (rank 0
+only).
 """
 from __future__ import annotations
 
@@ -67,11 +78,9 @@ def speedup_vs_standard(d, m, dv, N=None) -> float:
 
 # ------------------------------------------------------------------ multi-GPU host logic
 def shard_range(total: int, world: int, rank: int):
-    """Contiguous share [lo, hi) of `total` independent units (batch entries or
-    (b, h) pairs) owned by `rank`; shares differ in size by at most one."""
-    base, extra = divmod(total, world)
-    lo = rank * base + min(rank, extra)
-    return lo, lo + base + (1 if rank < extra else 0)
+    """Contiguous share [lo, hi) of `total` independent units owned by `rank`."""
+    from projected_feature_efficient_gb300.shard import shard_range as _sr
+    return _sr(total, world, rank)
 
 
 def max_over_ranks(x: float, dist=None, device=None) -> float:
@@ -241,22 +250,53 @@ def oracle_sample(w, q, k, v, P, target_s: float):
 
 
 # ------------------------------------------------------------------ arms
-def workload(heads=None, m=32):
-    """The C4 workload (optionally with fewer heads, for profiling captures)."""
+FWD_CONFIGS = ("C1", "C2", "C3", "C4", "C5", "C5ctl")
+# every point of the metric's sweep over N and m: (workload, m)
+SWEEP = (("C1", None), ("C2", None), ("C3", None), ("C4", 16), ("C4", 32), ("C4", 64),
+         ("C5", None), ("C5ctl", None))
+
+
+def workload(name="C4", heads=None, m=None):
+    """A forward workload by name, optionally with fewer heads (smaller case
+    for profiler captures); m picks a point of C4's projection-width sweep."""
     import spa_inputs as si
-    w = si.WORKLOADS["C4"].with_m(m)
+    w = si.WORKLOADS[name]
+    if m is not None and m != w.m:
+        if name != "C4":
+            raise SystemExit("--m applies to C4 only (its sweep is m in 16, 32, 64)")
+        w = w.with_m(m)
     return w.scaled(H=heads) if heads else w
 
 
-def config_of(w, world):
+def input_bytes(w) -> int:
+    es = 4 if w.dtype == "f32" else 2
+    return w.B * w.H * w.N * (2 * w.d + w.dv) * es
+
+
+def describe(w) -> str:
+    import spa_inputs as si
+    full = si.WORKLOADS[w.name]
+    qk = "rows rescaled to L2 norm sqrt(d)" if w.qk == "norm" else "iid N(0,1)"
+    proj = "P = I (exact-attention control)" if w.identity_P else "P iid N(0,1/m) per head"
+    return (f"{w.name}{'' if w.H == full.H else '-subset'}: B={w.B} H={w.H} N={w.N} d={w.d} "
+            f"m={w.m} d_v={w.dv} {w.dtype} {'causal' if w.causal else 'non-causal'}; "
+            f"Q,K {qk}; V iid N(0,1); {proj}")
+
+
+def config_of(w, world, flush=False, repeats=1, l2=None):
+    l2_mb = (l2 or 0) / 1e6
     return {
-        "workload": f"C4{'' if w.H == 32 else '-subset'}: B={w.B} H={w.H} N={w.N} d={w.d} m={w.m} d_v={w.dv} bf16 "
-                    f"{'causal' if w.causal else 'non-causal'}; Q,K,V iid N(0,1); "
-                    f"P iid N(0,1/m) per head",
+        "workload": describe(w),
         "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "d_v": w.dv, "causal": w.causal,
-        "l2": "inputs (805 MB) larger than L2 (129 MB); no flush between steps",
+        "l2": (f"inputs ({input_bytes(w) / 1e6:.0f} MB) smaller than L2 ({l2_mb:.0f} MB): a "
+               f"buffer of twice L2 is written between forwards, outside the timed events"
+               if flush else
+               f"inputs ({input_bytes(w) / 1e6:.0f} MB) larger than L2 ({l2_mb:.0f} MB); "
+               f"no flush between forwards"),
+        "repeats_per_step": repeats,
         "api": "spa_attention_prepare + spa_attention_apply on a preallocated workspace",
-        "parallelism": f"dp{world} (one independent copy of the workload per GPU)",
+        "parallelism": (f"dp{world}: the B*H (batch, head) pairs of one problem split across "
+                        f"ranks, no data-path collective") if world > 1 else "dp1",
     }
 
 
@@ -264,7 +304,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import spa_inputs as si
-    w = workload(args.heads, args.m)
+    w = workload(args.config, args.heads, args.m)
     q, k, v = si.make_qkv(w)
     P = si.make_P(w)
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -292,91 +332,135 @@ def run_reference(args, rank, world):
     return 0
 
 
-def run_ours(args, rank, world, local_rank):
+def fp32_fma_peak(sms: int) -> float:
+    """fp32 FMA roofline in TFLOP/s: 128 FMA lanes per SM per clock, 2 FLOPs
+    each, at the maximum SM clock."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", 2070.0))
+    except (OSError, ValueError):
+        mhz = 2070.0
+    return 2.0 * 128 * sms * mhz * 1e6 / 1e12
+
+
+def measure_forward(args, w, rank, world, dev, dist):
+    """One JSON line (rank 0) for the forward on workload w."""
     import torch
-    import torch.distributed as dist
 
     import projected_feature_efficient_gb300 as spa
     import spa_inputs as si
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    w = workload(args.heads, args.m)
-    lo, _ = shard_range(world * w.B, world, rank)
-    q_h, k_h, v_h = si.make_qkv(w, seed=None if lo == 0 else 1000 + w.number + 7919 * lo)
+    q_h, k_h, v_h = si.make_qkv(w)
     P_h = si.make_P(w)
+    # rank r computes its own contiguous share of the problem's (batch, head)
+    # pairs (the heads are independent); the shares of all ranks make up the
+    # whole problem, so the throughput is that of the whole job
+    if world > 1:
+        from projected_feature_efficient_gb300.shard import shard_pairs
+        _, _, q_h, k_h, v_h, P_h = shard_pairs(q_h, k_h, v_h, P_h, world, rank)
+    Bl, Hl = q_h.shape[0], q_h.shape[1]
     q, k, v, P = (t.to(dev) for t in (q_h, k_h, v_h, P_h))
-    B, H, N, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
-    ws = torch.empty(spa.spa_attention_workspace_size(B, H, N, d, m, dv, spa.SPA_BF16),
-                     dtype=torch.uint8, device=dev)
-    out = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    N, d, m, dv = w.N, w.d, w.m, w.dv
+    dcode = spa.SPA_F32 if w.dtype == "f32" else spa.SPA_BF16
+    nbytes = spa.spa_attention_workspace_size(Bl, Hl, N, d, m, dv, dcode)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((Bl, Hl, N, dv), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 1024 * 1024)
+    flush = input_bytes(w) < l2
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev) if flush else None
 
-    def step():
+    def prepare():
         spa.spa_attention_prepare(q, k, P, dv, ws)
-        spa.spa_attention_apply(v, ws, B, H, N, d, m, causal=w.causal, out=out)
+
+    def apply():
+        spa.spa_attention_apply(v, ws, Bl, Hl, N, d, m, causal=w.causal, out=out)
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def timed_region(sampler):
-        K = args.steps
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 1)]
-        barrier()
-        sampler.mark_start()
-        ev[0].record(stream)
-        for i in range(K):
-            spa.spa_attention_prepare(q, k, P, dv, ws)
-            ev[2 * i + 1].record(stream)
-            spa.spa_attention_apply(v, ws, B, H, N, d, m, causal=w.causal, out=out)
-            ev[2 * i + 2].record(stream)
-        barrier()
-        sampler.mark_end()
-        total = ev[0].elapsed_time(ev[2 * K])
-        attn = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(K))
-        proj = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(K))
-        return total, attn, proj
-
-    for _ in range(max(3, args.warmup)):
-        step()
+    W = max(3, args.warmup)
+    for i in range(W):
+        prepare()
+        apply()
+        if flush:
+            flush_buf.fill_(i & 255)
     torch.cuda.synchronize(dev)
     if spa.device_error() != 0:
         raise RuntimeError("a kernel gave up on a bounded wait during warm-up")
+    # repeats per step, so that the timed region lasts at least --min-seconds
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(3):
+        prepare()
+        apply()
+        if flush:
+            flush_buf.fill_(i & 255)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_iter = max(e0.elapsed_time(e1) / 3 * 1e-3, 1e-6)
+    K = args.steps
+    R = max(1, math.ceil(args.min_seconds / (K * t_iter)))
+    R = min(R, max(1, 20000 // K))
+    n = K * R
 
-    sampler = ClockSampler(physical_device(local_rank))
+    def timed_region(sampler):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * n)]
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        sampler.mark_start()
+        r0.record(stream)
+        for i in range(n):
+            ev[3 * i].record(stream)
+            prepare()
+            ev[3 * i + 1].record(stream)
+            apply()
+            ev[3 * i + 2].record(stream)
+            if flush:
+                flush_buf.fill_(i & 255)
+        r1.record(stream)
+        barrier()
+        sampler.mark_end()
+        fwd = sum(ev[3 * i].elapsed_time(ev[3 * i + 2]) for i in range(n))
+        attn = sum(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(n))
+        return fwd, attn, fwd - attn, r0.elapsed_time(r1)
+
+    sampler = ClockSampler(physical_device(dev.index))
     time.sleep(0.3)
-    total, attn, proj = timed_region(sampler)
+    fwd, attn, proj, region = timed_region(sampler)
     clocks = sampler.summary()
     remeasured = False
     if clocks and BAD_REASONS & set(clocks["reasons"]):
         sampler.stop()
-        sampler = ClockSampler(physical_device(local_rank))
+        sampler = ClockSampler(physical_device(dev.index))
         time.sleep(0.3)
-        total, attn, proj = timed_region(sampler)
+        fwd, attn, proj, region = timed_region(sampler)
         clocks = sampler.summary()
         remeasured = True
     sampler.stop()
+    if spa.device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
 
-    t_max_ms = max_over_ranks(total, dist, dev)
-    K = args.steps
-    f_step = flops(B, H, N, d, m, dv, w.causal)
-    value = world * f_step * K / (t_max_ms * 1e-3) / 1e12
+    fwd_max_ms = max_over_ranks(fwd, dist, dev)
+    f_all = flops(w.B, w.H, N, d, m, dv, w.causal)  # the whole problem, all ranks
+    value = f_all * n / (fwd_max_ms * 1e-3) / 1e12
 
-    # ---- end to end through the public host-buffer entry point
+    # ---- end to end through the public host-buffer entry point (this rank's share)
     qp, kp, vp, Pp = (x.pin_memory() for x in (q_h, k_h, v_h, P_h))
-    out_h = torch.empty((B, H, N, dv), dtype=torch.float32).pin_memory()
+    out_h = torch.empty((Bl, Hl, N, dv), dtype=torch.float32).pin_memory()
+    t0 = time.perf_counter()
     spa.spa_attention_fwd_host(qp, kp, vp, Pp, causal=w.causal, out=out_h)
-    Ke = max(1, min(K, 10))
+    t_one = max(time.perf_counter() - t0, 1e-6)
+    Ke = int(max(3, min(2000, math.ceil(0.5 / t_one))))
     barrier()
     t0 = time.perf_counter()
     for _ in range(Ke):
         spa.spa_attention_fwd_host(qp, kp, vp, Pp, causal=w.causal, out=out_h)
     te = max_over_ranks(time.perf_counter() - t0, dist, dev)
-    e2e_value = world * f_step * Ke / te / 1e12
+    e2e_value = f_all * Ke / te / 1e12
     h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, Pp))
     d2h = out_h.numel() * out_h.element_size()
     if spa.device_error() != 0:
@@ -387,36 +471,96 @@ def run_ours(args, rank, world, local_rank):
         fl, dt, desc, threads = oracle_sample(w, q_h, k_h, v_h, P_h, args.cpu_seconds)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": desc}
+    if rank != 0:
+        return None
+    peak, peak_sus, peak_src = load_peaks()
+    attn_ms = attn / n
+    a_fl = attn_flops(Bl, Hl, N, m, dv, w.causal)
+    achieved = a_fl / (attn_ms * 1e-3) / 1e12
+    if w.dtype == "f32":
+        fpk = fp32_fma_peak(props.multi_processor_count)
+        roof = {"bound": "alu", "achieved": achieved, "peak": fpk, "unit": "TFLOP/s",
+                "frac": achieved / fpk, "traffic": None,
+                "kernel": "attn_f32_kernel (scores + softmax + PV in fp32 FMA)",
+                "peak_source": "fp32 FMA: 128 lanes/SM/clock x 2 FLOPs x SMs x max SM clock"}
+        pct = None
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "traffic": (recorded_traffic(f"{w.name}_m{m}") if world == 1 and
+                            Hl == workload(w.name, m=w.m).H else None),
+                "kernel": "attn_ws_kernel (scores + softmax + PV)",
+                "peak_source": f"{peak_src} bf16 burst",
+                "frac_of_sustained": achieved / peak_sus}
+        pct = 100.0 * value / world / peak
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": fwd_max_ms / K,
+        "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16",
+        "data": "synthetic",
+        "config": config_of(w, world, flush, R, l2),
+        "pct_of_peak": pct,
+        "roofline": roof,
+        "kernels_ms_per_forward": {"projection": proj / n, "attention": attn_ms},
+        "timed_region_ms": region,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "api": "spa_attention_fwd_host", "steps": Ke},
+        "gpu_launches": 2 * n,
+        "clocks": clocks,
+    }
+    if remeasured:
+        line["remeasured_after_throttle"] = True
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
 
-    if rank == 0:
-        peak, peak_sus, peak_src = load_peaks()
-        attn_ms = attn / K
-        achieved = attn_flops(B, H, N, m, dv, w.causal) / (attn_ms * 1e-3) / 1e12
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": t_max_ms / K,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": config_of(w, world),
-            "pct_of_peak": 100.0 * value / world / peak,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": recorded_traffic(f"C4_m{m}") if w.H == 32 else None,
-                         "kernel": "attn_ws_kernel (scores + softmax + PV)",
-                         "peak_source": f"{peak_src} bf16 burst",
-                         "frac_of_sustained": achieved / peak_sus},
-            "kernels_ms_per_step": {"projection": proj / K, "attention": attn_ms},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "api": "spa_attention_fwd_host",
-                    "steps": Ke},
-            "gpu_launches": 2 * K,
-            "clocks": clocks,
-        }
-        if remeasured:
-            line["remeasured_after_throttle"] = True
-        if cpu is not None:
-            line["cpu_baseline"] = cpu
-        print(json.dumps(line), flush=True)
+
+def results_done(path, key, src_hash):
+    """True if the results file already holds the line of `key` measured on the
+    current kernel source (a sweep resumes where it stopped)."""
+    try:
+        with open(path) as f:
+            for raw in f:
+                try:
+                    rec = json.loads(raw)
+                except ValueError:
+                    continue
+                if rec.get("sweep_key") == key and rec.get("kernel_source") == src_hash:
+                    return True
+    except OSError:
+        pass
+    return False
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if args.sweep:
+        points = [(c, m) for c, m in SWEEP]
+    else:
+        points = [(args.config, args.m if args.config == "C4" else None)]
+    src_hash = kernel_source_hash()
+    for name, m in points:
+        w = workload(name, args.heads, m)
+        key = f"{w.name}_m{w.m}"
+        if args.results and results_done(args.results, key, src_hash):
+            continue
+        line = measure_forward(args, w, rank, world, dev, dist)
+        if line is not None:
+            if args.sweep or args.results:
+                line["sweep_key"] = key
+                line["kernel_source"] = src_hash
+            print(json.dumps(line), flush=True)
+            if args.results:
+                with open(args.results, "a") as f:
+                    f.write(json.dumps(line) + "\n")
+        torch.cuda.empty_cache()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -854,10 +998,19 @@ def main(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=None,
-                    help="run C4 (or the C3 backward) with fewer heads (smaller case for "
-                         "profiler captures)")
+                    help="run the workload (or the C3 backward) with fewer heads (smaller "
+                         "case for profiler captures)")
+    ap.add_argument("--config", default="C4", choices=FWD_CONFIGS,
+                    help="forward workload (default C4)")
     ap.add_argument("--m", type=int, default=32, choices=(16, 32, 64),
                     help="projection width of the C4 sweep")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measure every forward workload and C4 m point, one line each")
+    ap.add_argument("--results", default=None,
+                    help="append each line to this JSONL file and skip the workloads it "
+                         "already holds for the current kernel source")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="shortest timed region (passes per step are repeated to reach it)")
     ap.add_argument("--decode", action="store_true",
                     help="measure the decode row (projected key cache, workload D1) instead")
     ap.add_argument("--sfa", action="store_true",

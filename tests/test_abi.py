@@ -121,6 +121,28 @@ def test_workspace_entry_point_checks_its_buffer(lib):
     assert lib.spa_attention_fwd_ws(*args, A, need - 1, None) == NOMEM
 
 
+def test_noalloc_entry_point_validates_first(lib):
+    """The allocation-free forward checks its arguments before it looks up its
+    scratch array (no CUDA call happens in any of these cases)."""
+    def call(q=A, k=A, v=A, P=A, out=A, B=1, H=2, N=256, d=128, m=32, dv=128, dtype=BF16):
+        return lib.spa_attention_fwd_noalloc(q, k, v, P, out, B, H, N, d, m, dv, 0, dtype, None)
+    assert call(q=None) == NULL
+    assert call(P=None) == NULL
+    assert call(out=None) == NULL
+    assert call(v=A + 8) == ALIGN
+    assert call(out=A + 4) == ALIGN
+    assert call(N=-1) == SHAPE
+    assert call(B=300, H=300) == SHAPE
+    assert call(dtype=5) == DTYPE
+    assert call(m=24) == UNSUPPORTED
+    assert call(dv=96) == UNSUPPORTED
+    # an empty problem returns before the scratch is looked up
+    assert call(q=None, k=None, v=None, P=None, out=None, N=0) == OK
+    assert call(q=None, k=None, v=None, P=None, out=None, B=0) == OK
+    # a workspace larger than the 64 MiB array
+    assert call(H=64, N=131072) == NOMEM
+
+
 def test_host_entry_point_validates_first(lib):
     assert lib.spa_attention_fwd_host(None, A, A, A, A, 1, 1, 8, 64, 16, 64, 0, BF16, None) == NULL
     assert lib.spa_attention_fwd_host(A, A, A, A, A, 1, 1, 8, 64, 20, 64, 0, BF16, None) == \

@@ -54,8 +54,9 @@ def test_staged_forward_replays_in_a_graph():
 
 
 def test_allocating_forward_replays_in_a_graph():
-    """spa_attention_fwd takes its workspace with cudaMallocAsync, which a
-    graph records as allocation nodes."""
+    """spa_attention_fwd takes its workspace from the library's own memory
+    pool with cudaMallocFromPoolAsync, which a graph records as allocation
+    and free nodes on that pool."""
     pkg = spa()
     q, k, v, P, _ = _inputs(m=16)
     ref = pkg.spa_attention_fwd(q, k, v, P, causal=False)
