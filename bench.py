@@ -304,7 +304,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import spa_inputs as si
-    w = workload(args.config, args.heads, args.m)
+    name = args.config or "C4"
+    w = workload(name, args.heads, args.m if name == "C4" else None)
     q, k, v = si.make_qkv(w)
     P = si.make_P(w)
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -544,7 +545,8 @@ def run_ours(args, rank, world, local_rank):
     if args.sweep:
         points = [(c, m) for c, m in SWEEP]
     else:
-        points = [(args.config, args.m if args.config == "C4" else None)]
+        name = args.config or "C4"
+        points = [(name, args.m if name == "C4" else None)]
     src_hash = kernel_source_hash()
     for name, m in points:
         w = workload(name, args.heads, m)
@@ -746,9 +748,8 @@ def run_backward(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w = si.WORKLOADS["C3"]
-    if args.heads:
-        w = w.scaled(H=args.heads)
+    name = args.config if args.config in ("C3", "C4") else "C3"
+    w = workload(name, args.heads, args.m if name == "C4" else None)
     B, H, N, d, m, dv = w.B, w.H, w.N, w.d, w.m, w.dv
     q_h, k_h, v_h = si.make_qkv(w, seed=None if rank == 0 else 1000 + w.number + 7919 * rank)
     P_h = si.make_P(w)
@@ -827,12 +828,13 @@ def run_backward(args, rank, world, local_rank):
             "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": t_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"C3 backward: B={B} H={H} N={N} d={d} m={m} d_v={dv} bf16 "
-                                   f"causal; upstream gradient iid N(0,1)",
-                       "B": B, "H": H, "N": N, "d": d, "m": m, "d_v": dv, "causal": True,
+            "config": {"workload": f"{w.name} backward: B={B} H={H} N={N} d={d} m={m} d_v={dv} "
+                                   f"bf16 {'causal' if w.causal else 'non-causal'}; upstream "
+                                   f"gradient iid N(0,1)",
+                       "B": B, "H": H, "N": N, "d": d, "m": m, "d_v": dv, "causal": w.causal,
                        "api": "spa_attention_bwd_prepare / _apply / _finish (forward output "
                               "and lse computed once, outside)",
-                       "l2": "inputs and workspace (q, k, v, dO, 207 MB workspace) exceed L2",
+                       "l2": "inputs and workspace (q, k, v, dO and the workspace) exceed L2",
                        "parallelism": f"dp{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
@@ -840,9 +842,9 @@ def run_backward(args, rank, world, local_rank):
                          "peak_source": f"{peak_src} bf16 burst",
                          "frac_of_sustained": achieved / peak_sus},
             "kernels_ms_per_step": {"bwd_ws_kernel": k_ms, "rest": t_ms / K - k_ms},
-            # ours per step: projection, statistics, the kernel, dQp split,
-            # [P_h | P_h], dP fold (plus library GEMMs and one memset)
-            "gpu_launches": 6 * K,
+            # ours per step: projection, statistics, the kernel, the finish
+            # (plus two memsets)
+            "gpu_launches": 4 * K,
             "clocks": clocks,
         }
         if cpu is not None:
@@ -1000,8 +1002,8 @@ def main(argv=None):
     ap.add_argument("--heads", type=int, default=None,
                     help="run the workload (or the C3 backward) with fewer heads (smaller "
                          "case for profiler captures)")
-    ap.add_argument("--config", default="C4", choices=FWD_CONFIGS,
-                    help="forward workload (default C4)")
+    ap.add_argument("--config", default=None, choices=FWD_CONFIGS,
+                    help="workload (forward default C4; --backward default C3)")
     ap.add_argument("--m", type=int, default=32, choices=(16, 32, 64),
                     help="projection width of the C4 sweep")
     ap.add_argument("--sweep", action="store_true",
@@ -1016,7 +1018,8 @@ def main(argv=None):
     ap.add_argument("--sfa", action="store_true",
                     help="measure the Sparse Feature Attention row (C4 shape, k=16) instead")
     ap.add_argument("--backward", action="store_true",
-                    help="measure the backward row (workload C3) instead")
+                    help="measure the backward row instead (workload C3, or --config C4 "
+                         "with --m)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode with another batch size (smaller case for profiler captures)")
     args = ap.parse_args(argv)

@@ -24,8 +24,8 @@
  *              keeps, per device: a memory pool for the workspaces it takes
  *              itself (what it has reserved stays reserved until
  *              spa_host_pool_trim), the device error word, the internal
- *              streams of spa_attention_fwd_host, a library GEMM handle, and
- *              the fixed scratch array of spa_attention_fwd_noalloc.
+ *              streams of spa_attention_fwd_host, and the fixed scratch array
+ *              of spa_attention_fwd_noalloc.
  *   stream     a cudaStream_t passed as void* (NULL = legacy default stream).
  *              Work is enqueued asynchronously; the return value reports
  *              argument errors and launch errors only.  Faults inside a kernel
@@ -215,29 +215,28 @@ SPA_API int spa_attention_fwd_lse(const void *q, const void *k, const void *v, c
  *   dS = A * (dO V^T - D) / sqrt(m), dQp = dS Kp, dKp = dS^T Qp, dV = A^T dO,
  *   dq = dQp P_h^T, dk = dKp P_h^T, dP_h = sum_b (q^T dQp + k^T dKp)
  * ("Sparse Projection Attention", Sec. 3.4.1; Algorithm 2 trains P through
- * these).  d <= 128; the other limits are the forward's.  Two implementations:
- *   fused (SPA_BF16, m in {16, 32}, d_v in {64, 128}; every pointer 16-byte
- *     aligned, else SPA_ERR_ALIGN): A and dS are recomputed tile by tile on
- *     the tensor cores from the forward's row log-sum-exp and never stored.
- *     The scores use the forward's own operands; P^T and dS are rounded to
- *     bf16 for their products (fp32 accumulation), dQp / dKp are carried
- *     into dq, dk, dP as bf16 hi + lo pairs.  spa_attention_bwd runs the
- *     forward once more for the log-sum-exp; spa_attention_bwd_lse takes it.
- *   materialised (other cases): A and dS for as many heads as fit in 8 GB at
- *     a time (2 N^2 floats per head), plain cuBLAS products (fp32
- *     accumulation; TF32 products for bf16 inputs, exact for their values;
- *     fp32 products for fp32 inputs).
- * Workspace on `stream`: the fused version's from the library's pool (as for
- * spa_attention_fwd), the materialised version's from cudaMallocAsync.  An
- * empty problem (B*H*N == 0) zeroes dP.
+ * these).  d <= 128; the other limits are the forward's; every pointer 16-byte
+ * aligned, else SPA_ERR_ALIGN.  Both implementations are flash-style: A and dS
+ * are recomputed from the forward's row log-sum-exp and never stored.
+ *   tensor cores (SPA_BF16, d in {64, 128}, m in {16, 32, 64}, d_v in
+ *     {64, 128}): A and dS tile by tile in tensor memory.  The scores use the
+ *     forward's own operands; P^T and dS are rounded to bf16 for their
+ *     products (fp32 accumulation), dQp / dKp are carried into dq, dk, dP as
+ *     bf16 hi + lo pairs (16 significant bits).
+ *   CUDA cores (every other shape: SPA_F32, or m = 128, or another d):
+ *     the same chain rule in fp32, one warp per key row (dV, dKp) and per
+ *     query row (dQp).
+ * spa_attention_bwd runs the forward once more for the log-sum-exp;
+ * spa_attention_bwd_lse takes it.  Workspace on `stream` from the library's
+ * pool (as for spa_attention_fwd).  An empty problem (B*H*N == 0) zeroes dP.
  */
 SPA_API int spa_attention_bwd(const void *q, const void *k, const void *v, const void *P,
                               const float *out, const void *dO, float *dq, float *dk, float *dv,
                               float *dP, int B, int H, int N, int d, int m, int d_v, int causal,
                               int dtype, void *stream);
 /* spa_attention_bwd_lse -- the same with the forward's lse ([B][H][N] fp32, as
- * written by spa_attention_fwd_lse; SPA_ERR_NULL if missing), so the fused
- * path skips its own forward.  The materialised path ignores lse. */
+ * written by spa_attention_fwd_lse; SPA_ERR_NULL if missing), so neither path
+ * runs its own forward. */
 SPA_API int spa_attention_bwd_lse(const void *q, const void *k, const void *v, const void *P,
                                   const float *out, const float *lse, const void *dO, float *dq,
                                   float *dk, float *dv, float *dP, int B, int H, int N, int d,
@@ -247,16 +246,15 @@ SPA_API int spa_attention_bwd_lse(const void *q, const void *k, const void *v, c
  * The fused backward in three stages on a caller-provided workspace (device,
  * 256-byte aligned, at least spa_attention_bwd_workspace_size() bytes; the
  * stages must run in order on one stream with the same sizes and workspace).
- * Fused shapes only (SPA_BF16, d <= 128, m in {16, 32}, d_v in {64, 128};
- * otherwise SPA_ERR_UNSUPPORTED); pointers 16-byte aligned.
+ * Tensor-core shapes only (SPA_BF16, d in {64, 128}, m in {16, 32, 64}, d_v
+ * in {64, 128}; otherwise SPA_ERR_UNSUPPORTED); pointers 16-byte aligned.
  *   prepare: the forward's score operands, bf16 Qp / Kp tiles, row statistics
  *            (D_i = <dO_i, out_i>, lse) and a zeroed dQp accumulator.
- *   apply:   the tensor-core kernel; writes dv and leaves dQp, dKp in the
- *            workspace.
- *   finish:  dq, dk, dP from dQp, dKp: one tensor-core pass for d = 128 and
- *            m = 32 (dP is summed with floating-point reduce-adds whose order
- *            may vary), library GEMMs otherwise.
- * prepare + apply + finish gives exactly spa_attention_bwd_lse.
+ *   apply:   the tensor-core kernel; writes dv and leaves dQp, dKp (fp32) in
+ *            the workspace.
+ *   finish:  dq, dk, dP from dQp, dKp in one tensor-core pass (dP is summed
+ *            with floating-point reduce-adds whose order may vary).
+ * prepare + apply + finish gives spa_attention_bwd_lse's dq, dk, dv bit for bit.
  */
 SPA_API int spa_attention_bwd_workspace_size(int B, int H, int N, int d, int m, int d_v,
                                              int dtype, size_t *bytes);

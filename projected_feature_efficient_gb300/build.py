@@ -70,12 +70,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(s) for s, _ in failed))
     tmp = LIB + f".tmp{os.getpid()}"
-    # cuBLAS (plain GEMMs of the backward) from the toolkit that compiled the
-    # kernels; the run path points there so the library loads without
-    # LD_LIBRARY_PATH
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
-    link = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o, _ in results], "-cudart", "static",
-            "-L", cuda_lib, "-lcublas", "-Xlinker", "-rpath," + cuda_lib]
+    # only the static CUDA runtime: every kernel is our own, no library GEMM
+    link = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o, _ in results], "-cudart", "static"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

@@ -9,6 +9,16 @@
 
 namespace spa {
 
+// Tile layout of the fp32 gradient accumulators dQp and dKp the fused kernel
+// writes and the finish kernel reads: per 128-row tile, m / W slabs of
+// 128 rows x W columns (W = dq_slab_cols(m)), one after the other; within a
+// slab, 16-byte chunk q of row e sits at chunk q ^ dq_slab_swizzle(e, W)
+// (which spreads a warp's row-per-thread accesses over the banks).
+__host__ __device__ constexpr int dq_slab_cols(int m) { return m > 32 ? 16 : m; }
+__host__ __device__ constexpr uint32_t dq_slab_swizzle(int e, int W) {
+  return static_cast<uint32_t>((e * W / 32) & (W / 4 - 1));
+}
+
 // Bulk reduce-add shared -> global (fp32 add, element-wise), tracked by bulk groups.
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(

@@ -26,16 +26,18 @@
 //                            product) and into a shared-memory tile in the
 //                            MN-major layout the dQp product reads (dS, M = queries).
 //   warps 16-19  epilogue: per query tile the column factors a_i, then the
-//                dQp tile out of TMEM, through a staging tile, into the
-//                reduce-add; per item the dV rows (fp32) and the dKp rows
-//                (bf16 hi | lo pairs, what the projection-gradient GEMMs read).
+//                dQp tile out of TMEM, through a staging tile (in slabs of at
+//                most 32 columns), into the reduce-add; per item the dV rows
+//                (fp32) and the dKp tile (fp32, the accumulators' tile layout).
 //   warp 20      loads (one thread): per item the key tile's score operand,
 //                its bf16 Kp tile and V; per query tile a two-slot ring of
 //                dO, the score operand, the bf16 Qp tile and the row statistics.
 //   warp 21      tensor-memory allocation; one thread issues S^T, dV and dQp.
 //   warp 22      one thread issues dP^T and dKp.
 //   warp 23      idle.
-// Tensor memory (512 columns): S^T | dP^T/dS^T | dV | dKp | dQp | P^T.
+// Tensor memory (512 columns): S^T | dP^T/dS^T | dV | dKp | dQp | P^T, or at
+// m = 64 with d_v = 128 (where that does not fit) S^T/P^T | dP^T/dS^T | dV |
+// dKp | dQp with each warpgroup's P^T pairs written over its own S^T columns.
 // Per query tile i the two issuing threads run
 //   X: S^T(i) = Kf Qf_i^T (first tile of an item; otherwise issued early)
 //      [S^T(i) in registers] S^T(i+1)      (over S^T(i))
@@ -96,17 +98,24 @@ struct BwdPlan {
   static constexpr int kVBytes = kTileRows * DV * 2;    // V or dO tile (64-column SW128 boxes)
   static constexpr int kStatBytes = 4 * kTileRows * 4;  // planes: qm, nl, dn, a
   static constexpr int kDsBytes = kTileRows * kTileRows * 2;
-  static constexpr int kDqBytes = kTileRows * MB * 4;
-  // ring stage: dO | Qf | Qb | stats, padded so every dO tile is 1024-aligned
+  // dQp leaves tensor memory in slabs of kDqSlab columns, one staging tile
+  // and one bulk reduce-add each (the accumulator's tile layout, bwd_common.cuh)
+  static constexpr int kDqSlab = dq_slab_cols(MB);
+  static constexpr int kDqSlabs = MB / kDqSlab;
+  static constexpr int kDqBytes = kTileRows * kDqSlab * 4;
+  // the bf16 Qp tile is read late in a query tile (dKp product); at m = 64 it
+  // is single-buffered (the next one loads during the next tile's first half)
+  static constexpr int kQbStages = MB > 32 ? 1 : 2;
+  // ring stage: dO | Qf | stats, padded so every dO tile is 1024-aligned
   static constexpr int kStDo = 0;
   static constexpr int kStQf = kVBytes;
-  static constexpr int kStQb = kStQf + kKfBytes;
-  static constexpr int kStStat = kStQb + kBBytes;
+  static constexpr int kStStat = kStQf + kKfBytes;
   static constexpr int kStageBytes = (kStStat + kStatBytes + 1023) / 1024 * 1024;
   static constexpr int kV = 0;
   static constexpr int kDs = kV + kVBytes;
   static constexpr int kRing = kDs + kDsBytes;
-  static constexpr int kKf = kRing + 2 * kStageBytes;
+  static constexpr int kQb = kRing + 2 * kStageBytes;
+  static constexpr int kKf = kQb + kQbStages * kBBytes;
   static constexpr int kKb = kKf + kKfBytes;
   static constexpr int kDq = kKb + kBBytes;
   static constexpr int kBytes = kDq + kDqBytes;
@@ -114,10 +123,16 @@ struct BwdPlan {
   static_assert(kLaunch <= kBMaxDynSmem, "backward shared-memory plan too large");
   static_assert(kVBytes % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024 alignment");
   // S^T | dP^T/dS^T | dV | dKp | dQp | P^T (bf16 pairs: the pair of queries
-  // 2c, 2c+1 in column c, so k-step k of the dV product reads columns 8k ..)
+  // 2c, 2c+1 in column c, so k-step k of the dV product reads columns 8k ..).
+  // Where that does not fit (m = 64 with d_v = 128), P^T is written over the
+  // S^T columns of each warpgroup (k-step k reads pair_col(k)), and the next
+  // S^T is issued only after the dV product has read P^T.
+  static constexpr bool kPOverS = 256 + DV + 2 * MB + 64 > 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + DV,
-                            kColDQ = 256 + DV + MB, kColP = 256 + DV + 2 * MB;
-  static_assert(kColP + 64 <= 512, "tensor-memory plan too large");
+                            kColDQ = 256 + DV + MB,
+                            kColP = kPOverS ? 0u : 256 + DV + 2 * MB;
+  static_assert(kColDQ + MB <= 512 && (kPOverS || kColP + 64 <= 512),
+                "tensor-memory plan too large");
 };
 
 struct BwdBars {
@@ -171,7 +186,8 @@ __device__ __forceinline__ void bwd_loader(const BwdTcParams& p, const CUtensorM
                                            const WaitCtl& ctl, int items) {
   prefetch_tmap(vmap);
   prefetch_tmap(domap);
-  uint32_t g = 0;  // query tiles armed so far
+  uint32_t g = 0;   // query tiles so far
+  uint32_t ga = 0, gb = 0;  // query tiles whose part A / part B loads were started
   int karmed = 0;  // items armed so far
   bool ok = true;
   for (int k = 0; ok; ++k) {
@@ -205,19 +221,26 @@ __device__ __forceinline__ void bwd_loader(const BwdTcParams& p, const CUtensorM
       bulk_g2s(st + Plan::kStQf, p.Qs + qtile * kTileRows * KD, Plan::kKfBytes, &bars.qa_full[s]);
       bulk_g2s(st + Plan::kStStat, p.stats + qtile * 4 * kTileRows, Plan::kStatBytes,
                &bars.qa_full[s]);
-      if (g >= 2 && !(ok = wait_or_abort(&bars.qb_empty[s], ((g >> 1) - 1) & 1, ctl))) break;
-      mbar_arrive_expect_tx(&bars.qb_full[s], Plan::kBBytes);
-      bulk_g2s(st + Plan::kStQb, p.Qb + qtile * kTileRows * MB, Plan::kBBytes, &bars.qb_full[s]);
+      ga = g + 1;
+      constexpr int QS = Plan::kQbStages;
+      const int sb = QS == 2 ? s : 0;
+      if (g >= QS && !(ok = wait_or_abort(&bars.qb_empty[sb], ((g / QS) - 1) & 1, ctl))) break;
+      mbar_arrive_expect_tx(&bars.qb_full[sb], Plan::kBBytes);
+      bulk_g2s(smem + Plan::kQb + sb * Plan::kBBytes, p.Qb + qtile * kTileRows * MB,
+               Plan::kBBytes, &bars.qb_full[sb]);
+      gb = g + 1;
     }
   }
   // every copy this thread started lands before the CTA's memory is released
   if (karmed > 0) mbar_wait(&bars.kv_full, (karmed - 1) & 1, ctl.limit_ns);
   for (uint32_t s = 0; s < 2; ++s) {
-    const uint32_t n = g > s ? (g - s + 1) / 2 : 0;  // times stage s was armed
-    if (n > 0) {
-      mbar_wait(&bars.qa_full[s], (n - 1) & 1, ctl.limit_ns);
-      mbar_wait(&bars.qb_full[s], (n - 1) & 1, ctl.limit_ns);
-    }
+    const uint32_t n = ga > s ? (ga - s + 1) / 2 : 0;  // times stage s was armed
+    if (n > 0) mbar_wait(&bars.qa_full[s], (n - 1) & 1, ctl.limit_ns);
+  }
+  constexpr uint32_t QS = Plan::kQbStages;
+  for (uint32_t s = 0; s < QS; ++s) {
+    const uint32_t n = gb > s ? (gb - s + QS - 1) / QS : 0;  // times Qb buffer s was armed
+    if (n > 0) mbar_wait(&bars.qb_full[s], (n - 1) & 1, ctl.limit_ns);
   }
 }
 
@@ -251,7 +274,8 @@ struct BwdDescs {
     for (int s = 0; s < 2; ++s) {
       const uint32_t st = sbase + Plan::kRing + s * Plan::kStageBytes;
       Qf[s] = smem_desc(st + Plan::kStQf, 2048, 128, kLayoutInterleave);
-      Qb[s] = smem_desc(st + Plan::kStQb, 128, 2048, kLayoutInterleave);
+      Qb[s] = smem_desc(sbase + Plan::kQb + (s % Plan::kQbStages) * Plan::kBBytes, 128, 2048,
+                        kLayoutInterleave);
       DoK[s] = smem_desc(st + Plan::kStDo, 16, 1024, kLayoutSwizzle128);
       DoM[s] = smem_desc(st + Plan::kStDo, 16384, 1024, kLayoutSwizzle128);
     }
@@ -277,9 +301,10 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
   auto issue_dv = [&](int s, uint32_t acc) {  // dV += P^T dO, depth = 128 queries
     const uint64_t b = s ? dsc.DoM[1] : dsc.DoM[0];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      mma_ts(tb + Plan::kColDV, tb + Plan::kColP + 8 * k, b + (k * 2048 >> 4), D::kIdDV,
-             k > 0 ? 1u : acc);
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t a = Plan::kPOverS ? Plan::kColS + pair_col(k) : Plan::kColP + 8 * k;
+      mma_ts(tb + Plan::kColDV, tb + a, b + (k * 2048 >> 4), D::kIdDV, k > 0 ? 1u : acc);
+    }
   };
   auto issue_dq = [&]() {  // dQp = dS Kb, depth = 128 keys
 #pragma unroll
@@ -300,7 +325,7 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
         tc_fence_after();
         issue_s(s);
       }
-      if (n + 1 < it.nq) {
+      if (!Plan::kPOverS && n + 1 < it.nq) {
         // the next tile's scores as soon as the gradient warps hold S^T(i)
         // in registers: they overwrite nothing else
         const int s1 = (g + 1) & 1;
@@ -318,6 +343,14 @@ __device__ __forceinline__ void bwd_issuer_x(const BwdTcParams& p, uint32_t sbas
       issue_dv(s, n > 0 ? 1u : 0u);
       mma_commit(&bars.dv_done);     // P^T(i) is read: the P columns are free
       mma_commit(&bars.qa_empty[s]);  // X is done with part A of stage s (Qf, dO)
+      if (Plan::kPOverS && n + 1 < it.nq) {
+        // P^T(i) sits in the S^T columns: the next scores follow the dV
+        // product that reads it, in this thread's order
+        const int s1 = (g + 1) & 1;
+        if (!(ok = wait_or_abort(&bars.qa_full[s1], ((g + 1) >> 1) & 1, ctl))) break;
+        tc_fence_after();
+        issue_s(s1);
+      }
       if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl))) break;
       if (g > 0 && !(ok = wait_or_abort(&bars.dq_empty, (g - 1) & 1, ctl))) break;
       tc_fence_after();
@@ -346,8 +379,8 @@ __device__ __forceinline__ void bwd_issuer_y(const BwdTcParams& p, uint32_t sbas
     }
     mma_commit(&bars.dp_full);
   };
-  auto issue_dk = [&](int s, uint32_t acc) {  // dKp += dS^T Qb
-    const uint64_t b = s ? dsc.Qb[1] : dsc.Qb[0];
+  auto issue_dk = [&](int sb, uint32_t acc) {  // dKp += dS^T Qb
+    const uint64_t b = sb ? dsc.Qb[1] : dsc.Qb[0];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       mma_ts(tb + Plan::kColDK, tb + Plan::kColDP + pair_col(k), b + (k * 256 >> 4), D::kIdDK,
@@ -366,13 +399,15 @@ __device__ __forceinline__ void bwd_issuer_y(const BwdTcParams& p, uint32_t sbas
       tc_fence_after();
       issue_dp(s);  // overwrites dS^T(i-1) after dKp(i-1), in this thread's order
       mma_commit(&bars.qa_empty[s]);  // Y is done with part A of stage s (dO)
+      constexpr uint32_t QS = Plan::kQbStages;
+      const int sb = QS == 2 ? s : 0;
       if (!(ok = wait_or_abort(&bars.ds_full, g & 1, ctl) &&
-                 wait_or_abort(&bars.qb_full[s], (g >> 1) & 1, ctl)))
+                 wait_or_abort(&bars.qb_full[sb], (g / QS) & 1, ctl)))
         break;
       if (n == 0 && k > 0 && !(ok = wait_or_abort(&bars.acc_empty, (k - 1) & 1, ctl))) break;
       tc_fence_after();
-      issue_dk(s, n > 0 ? 1u : 0u);
-      mma_commit(&bars.qb_empty[s]);  // part B of stage s (Qb) is read
+      issue_dk(sb, n > 0 ? 1u : 0u);
+      mma_commit(&bars.qb_empty[sb]);  // the bf16 Qp tile is read
     }
     if (!ok) break;
     mma_commit(&bars.kv_empty);
@@ -393,7 +428,9 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
   const int r = (warp & 3) * 32 + lane;     // key row of the tile == TMEM lane
   const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const uint32_t tS = lane_base + Plan::kColS + C * wg;
-  const uint32_t tP = lane_base + Plan::kColP + (C / 2) * wg;
+  // P^T pairs: in a region of their own (16 columns per warpgroup), or over
+  // this warpgroup's own S^T columns
+  const uint32_t tP = lane_base + (Plan::kPOverS ? Plan::kColS + C * wg : Plan::kColP + (C / 2) * wg);
   const uint32_t tDP = lane_base + Plan::kColDP + C * wg;
   // this row of the dS tile: half (C wg) / 64, first 16-byte chunk (C wg % 64) / 8
   const uint32_t srow = sbase + Plan::kDs + (C * wg / 64) * 16384 + r * 128;
@@ -421,9 +458,11 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
 #pragma unroll
       for (int h = 0; h < NH; ++h) tmem_ld32(tS + 32 * h, x[h]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free);  // the next S^T may overwrite these columns
+      if constexpr (!Plan::kPOverS) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.s_free);  // the next S^T may overwrite these columns
+      }
       // query column c (of this warpgroup's C) is visible to key row r unless
       // the causal mask hides it on the diagonal tile; padded key rows see nothing
       const int cmin = !row_ok ? C : ((p.causal && qt == it.kt) ? r - C * wg : 0);
@@ -530,11 +569,11 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
                                              int items, int warp, int lane) {
   const int e = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQp), key row (dV, dKp)
   const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-  constexpr int kChunks = MB / 4;  // 16-byte chunks per dQp row
-  // swizzle of the staging tile (and of the dQp accumulator's tiles): chunk q of
-  // row e sits at q ^ (128-byte line of the row % kChunks)
-  const uint32_t dsw = static_cast<uint32_t>((e * MB / 32) & (kChunks - 1));
-  const uint32_t stage_row = sbase + Plan::kDq + e * MB * 4;
+  // the accumulators' tile layout (bwd_common.cuh): slabs of W columns, chunk
+  // q of row e at q ^ dsw; the staging tile holds one slab
+  constexpr int W = Plan::kDqSlab;
+  const uint32_t dsw = dq_slab_swizzle(e, W);
+  const uint32_t stage_row = sbase + Plan::kDq + e * W * 4;
 
   // the column factors a_i = (Q row multiplier) x (K tile multiplier) of tile gg
   auto cook = [&](uint32_t gg, const BItem& itc) -> bool {
@@ -566,29 +605,36 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
       // the four warps decide together, so that they meet the barriers below as one
       if (!(ok = named_bar_and(kEpiBar, 128, ok))) break;
       tc_fence_after();
-      if (e == 0) bulk_wait_group_read<0>();  // the previous reduce has read the staging tile
-      named_bar_sync(kEpiBar, 128);
-      // 16 columns (4 chunks) at a time: TMEM -> staging row
+      const size_t qtile = static_cast<size_t>(it.bh) * p.NT + it.qt0 + n;
 #pragma unroll
-      for (int c16 = 0; c16 < MB / 16; ++c16) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + Plan::kColDQ + 16 * c16, v);
-        tmem_wait_ld();
+      for (int sl = 0; sl < Plan::kDqSlabs; ++sl) {
+        if (e == 0) bulk_wait_group_read<0>();  // the previous reduce has read the staging tile
+        named_bar_sync(kEpiBar, 128);
+        // 16 columns (4 chunks) at a time: TMEM -> staging row
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t q = static_cast<uint32_t>(4 * c16 + j);
-          st_shared_v4(stage_row + ((q ^ dsw) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int c16 = 0; c16 < W / 16; ++c16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + Plan::kColDQ + sl * W + 16 * c16, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t q = static_cast<uint32_t>(4 * c16 + j);
+            st_shared_v4(stage_row + ((q ^ dsw) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+          }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.dq_empty);
-      fence_proxy_async_smem();
-      named_bar_sync(kEpiBar, 128);
-      if (e == 0) {
-        const size_t qtile = static_cast<size_t>(it.bh) * p.NT + it.qt0 + n;
-        bulk_reduce_add_f32(p.dqacc + qtile * kTileRows * MB, sbase + Plan::kDq, Plan::kDqBytes);
-        bulk_commit_group();
+        if (sl == Plan::kDqSlabs - 1) {  // dQp is read out: the next product may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.dq_empty);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(kEpiBar, 128);
+        if (e == 0) {
+          bulk_reduce_add_f32(p.dqacc + (qtile * Plan::kDqSlabs + sl) * kTileRows * W,
+                              sbase + Plan::kDq, Plan::kDqBytes);
+          bulk_commit_group();
+        }
       }
     }
     if (!ok) break;
@@ -598,24 +644,21 @@ __device__ __forceinline__ void bwd_epilogue(const BwdTcParams& p, uint8_t* smem
     tc_fence_after();
     const int row = it.kt * kTileRows + e;
     const bool wr = row < p.N;
-    // dKp as bf16 pairs: [hi (m values) | lo (m values)], 16 columns at a time
-    uint4* kdst = reinterpret_cast<uint4*>(p.xk + (static_cast<size_t>(it.bh) * p.N + row) * 2 * MB);
+    // dKp (fp32) into its tile of the accumulator layout, every row of the
+    // tile (padded key rows hold zeros: their probabilities are masked)
+    float* ktile = p.dkacc + (static_cast<size_t>(it.bh) * p.NT + it.kt) * kTileRows * MB;
 #pragma unroll
     for (int c16 = 0; c16 < MB / 16; ++c16) {
       uint32_t v[16];
       tmem_ld16(lane_base + Plan::kColDK + 16 * c16, v);
       tmem_wait_ld();
-      if (wr) {
+      const int sl = 16 * c16 / W;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            split_pair(__uint_as_float(v[8 * q + 2 * i]), __uint_as_float(v[8 * q + 2 * i + 1]),
-                       hi[i], lo[i]);
-          kdst[2 * c16 + q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          kdst[MB / 8 + 2 * c16 + q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t q = static_cast<uint32_t>((16 * c16 % W) / 4 + j);
+        *reinterpret_cast<float4*>(ktile + (sl * kTileRows + e) * W + ((q ^ dsw) << 2)) =
+            make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
       }
     }
     float4* dvrow = reinterpret_cast<float4*>(p.dv_out + (static_cast<size_t>(it.bh) * p.N + row) * DV);
@@ -736,6 +779,7 @@ template <int DV>
 cudaError_t launch_bwd_dv(const BwdTcParams& p, cudaStream_t stream) {
   if (p.m == 16 && !p.f16_ops && p.KD == 48) return launch_bwd<48, 16, DV, false>(p, stream);
   if (p.m == 32 && p.f16_ops && p.KD == 32) return launch_bwd<32, 32, DV, true>(p, stream);
+  if (p.m == 64 && p.f16_ops && p.KD == 64) return launch_bwd<64, 64, DV, true>(p, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -840,51 +884,11 @@ __global__ void __launch_bounds__(128) bwd_stats_tma_kernel(
   }
 }
 
-// (bh, i, 4-column group) of dQp, i < N: its swizzled tile chunk -> bf16 hi | lo row
-__global__ void bwd_split_kernel(const float* __restrict__ dqacc, uint16_t* __restrict__ xq, int BH,
-                                 int N, int NT, int m) {
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int chunks = m / 4;
-  const long long total = static_cast<long long>(BH) * N * chunks;
-  if (t >= total) return;
-  const int q = static_cast<int>(t % chunks);
-  const long long row = t / chunks;  // bh * N + i
-  const int bh = static_cast<int>(row / N), i = static_cast<int>(row % N);
-  const int e = i % kTileRows;
-  const int phys = q ^ ((e * m / 32) & (chunks - 1));
-  const float4 v = __ldg(reinterpret_cast<const float4*>(
-      dqacc + ((static_cast<size_t>(bh) * NT + i / kTileRows) * kTileRows + e) * m + phys * 4));
-  uint32_t hi0, lo0, hi1, lo1;
-  split_pair(v.x, v.y, hi0, lo0);
-  split_pair(v.z, v.w, hi1, lo1);
-  uint16_t* dst = xq + static_cast<size_t>(row) * 2 * m + 4 * q;
-  *reinterpret_cast<uint2*>(dst) = make_uint2(hi0, hi1);
-  *reinterpret_cast<uint2*>(dst + m) = make_uint2(lo0, lo1);
-}
-
-__global__ void bwd_dup_p_kernel(const __nv_bfloat16* __restrict__ P, uint16_t* __restrict__ P2,
-                                 long long n, int m) {
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n) return;  // n = H * d * 2m
-  const int c2 = static_cast<int>(t % (2 * m));
-  const long long hl = t / (2 * m);
-  P2[t] = __bfloat16_as_ushort(P[hl * m + c2 % m]);
-}
-
-__global__ void bwd_fold_kernel(const float* __restrict__ R, float* __restrict__ dP, long long n,
-                                int m) {
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n) return;  // n = H * d * m
-  const int c = static_cast<int>(t % m);
-  const long long hl = t / m;
-  dP[t] = R[hl * 2 * m + c] + R[hl * 2 * m + m + c];
-}
-
-unsigned blocks_for(long long n, int per) { return static_cast<unsigned>((n + per - 1) / per); }
-
 }  // namespace
 
-bool bwd_tc_supported(int m, int dv) { return (m == 16 || m == 32) && (dv == 64 || dv == 128); }
+bool bwd_tc_supported(int m, int dv) {
+  return (m == 16 || m == 32 || m == 64) && (dv == 64 || dv == 128);
+}
 
 cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream) {
   if (p.dv == 64) return launch_bwd_dv<64>(p, stream);
@@ -921,29 +925,6 @@ cudaError_t launch_bwd_stats(const BwdStatsMaps& maps, const float* lse, const f
   if (dv == 128) return launch_bwd_stats_tma<128>(maps, lse, qmul, stats, BH, N, NT, alpha, stream);
   if (dv == 64) return launch_bwd_stats_tma<64>(maps, lse, qmul, stats, BH, N, NT, alpha, stream);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, int NT, int m,
-                             cudaStream_t stream) {
-  const long long n = static_cast<long long>(BH) * N * (m / 4);
-  if (n == 0) return cudaSuccess;
-  bwd_split_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(dqacc, xq, BH, N, NT, m);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_dup_p(const __nv_bfloat16* P, uint16_t* P2, int H, int d, int m,
-                             cudaStream_t stream) {
-  const long long n = static_cast<long long>(H) * d * 2 * m;
-  if (n == 0) return cudaSuccess;
-  bwd_dup_p_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(P, P2, n, m);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_fold(const float* R, float* dP, int H, int d, int m, cudaStream_t stream) {
-  const long long n = static_cast<long long>(H) * d * m;
-  if (n == 0) return cudaSuccess;
-  bwd_fold_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(R, dP, n, m);
-  return cudaGetLastError();
 }
 
 }  // namespace spa

@@ -89,19 +89,7 @@ struct TopkParams {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream);  // P[h] = I_d
 
-// Gradients of the forward (materialised per head group, library GEMMs).
-struct BwdParams {
-  const void *q, *k, *v, *P, *dO;  // inputs (bf16 or fp32), same layouts as the forward
-  const float* out;                 // the forward's output [BH][N][dv]
-  float *dq, *dk, *dv_out, *dP;     // gradients: [BH][N][d], [BH][N][d], [BH][N][dv], [H][d][m]
-  int B, H, N, d, m, dv, causal, bf16;
-  int group;                        // heads whose N x N blocks are in memory at once
-};
-size_t backward_workspace_bytes(const BwdParams& p);
-int backward_group(int B, int H, int N, size_t budget_bytes);
-int run_backward(const BwdParams& p, void* ws, cudaStream_t stream);  // 0, -1 CUDA, -2 cuBLAS
-
-// Fused backward on tcgen05 (bf16 inputs, m in {16, 32}, d_v in {64, 128}).
+// Fused backward on tcgen05 (bf16 inputs, m in {16, 32, 64}, d_v in {64, 128}).
 // Tiles are 128 rows; NT = ceil(N / 128).
 struct BwdTcParams {
   const uint16_t* Qs;    // [BH][NT][128*KD] score-operand tiles, exactly the forward's
@@ -112,8 +100,9 @@ struct BwdTcParams {
   const float* stats;    // [BH][NT][4][128]: Q row multiplier, -lse*log2(e), -D/sqrt(m), 0
   CUtensorMap vmap;      // V  as 3-D (d_v, N, BH), bf16, 128-byte swizzle, box (64,128,1)
   CUtensorMap domap;     // dO as 3-D (d_v, N, BH), same encoding
-  float* dqacc;          // [BH][NT][128*m] fp32 dQp accumulator (zeroed; swizzled rows)
-  uint16_t* xk;          // [BH][N][2m] dKp rows as bf16 hi | lo
+  float* dqacc;          // [BH][NT][128*m] fp32 dQp accumulator (zeroed; tile layout of
+                         // bwd_common.cuh)
+  float* dkacc;          // [BH][NT][128*m] fp32 dKp, same tile layout
   float* dv_out;         // [BH][N][d_v] fp32 dV
   int* err;
   int BH, N, NT, KD, m, dv, causal;
@@ -135,33 +124,40 @@ struct BwdStatsMaps {
 cudaError_t launch_bwd_stats(const BwdStatsMaps& maps, const float* lse, const float* qmul,
                              float* stats, int BH, int N, int NT, int dv, float alpha,
                              cudaStream_t stream);
-// dQp (swizzled tiles) -> bf16 hi | lo rows [BH][N][2m]
-cudaError_t launch_bwd_split(const float* dqacc, uint16_t* xq, int BH, int N, int NT, int m,
-                             cudaStream_t stream);
-// P2[h] = [P_h | P_h] (bf16 [H][d][2m]);  dP[h][l][c] = R[h][l][c] + R[h][l][m + c]
-cudaError_t launch_bwd_dup_p(const __nv_bfloat16* P, uint16_t* P2, int H, int d, int m,
-                             cudaStream_t stream);
-cudaError_t launch_bwd_fold(const float* R, float* dP, int H, int d, int m, cudaStream_t stream);
-// The projection gradients in one pass on the tensor cores (m = 32, d = 128):
-// dq = dQp [P_h; P_h]^T-style products of the bf16 hi | lo split, dk likewise,
-// dP_h accumulated per head in tensor memory and bulk-added into dP.
+// The projection gradients in one pass on the tensor cores (d in {64, 128},
+// m in {16, 32, 64}): dq = dQp P_h^T and dk = dKp P_h^T from the bf16 hi | lo
+// split of the fp32 accumulators, dP_h accumulated per head in tensor memory
+// and bulk-added into dP.
 struct BwdFinishParams {
   CUtensorMap qmap, kmap;    // q, k as 3-D (d, N, BH), bf16, 128-byte swizzle, box (64,128,1)
-  CUtensorMap xkmap;         // dKp rows [BH][N][2m] bf16 hi | lo, same encoding (2m = 64)
   CUtensorMap dqmap, dkmap;  // dq, dk fp32 (d, N, BH), 128-byte swizzle, box (32,128,1)
-  const float* dqacc;        // [BH][NT][128*m] fp32 dQp accumulator (swizzled rows)
+  const float* dqacc;        // [BH][NT][128*m] fp32 dQp (tile layout of bwd_common.cuh)
+  const float* dkacc;        // [BH][NT][128*m] fp32 dKp, same layout
   const __nv_bfloat16* P;    // [H][d][m]
-  float* dP;                 // [H][d][m] fp32, zeroed before the launch
+  float* dP;                 // [H][d][m] fp32, zeroed by the launcher
   int* err;                  // device error word
   int B, H, N, NT, d, m;
   unsigned long long limit_ns;  // time limit of every wait in the kernel
 };
 bool bwd_finish_tc_supported(int d, int m);
 cudaError_t launch_bwd_finish_tc(const BwdFinishParams& p, cudaStream_t stream);
-// dq, dk, dP from the split dQp / dKp rows (library GEMMs on bf16, fp32 accumulation)
-int run_backward_post(const void* q, const void* k, const uint16_t* P2, const uint16_t* xq,
-                      const uint16_t* xk, float* R, float* dq, float* dk, float* dP, int B,
-                      int H, int N, int d, int m, cudaStream_t stream);
+
+// Backward on CUDA cores for the shapes the tensor-core kernels do not cover
+// (fp32 inputs; bf16 with m = 128): flash-style, the probabilities recomputed
+// from the forward's row log-sum-exp, never stored; fp32 arithmetic.
+struct BwdSimtParams {
+  const void *q, *k, *v, *P, *dO;  // inputs (bf16 or fp32), the forward's layouts
+  const float* out;                 // the forward's output [BH][N][dv]
+  const float* lse;                 // the forward's row log-sum-exp [BH][N] (natural log)
+  float *dq, *dk, *dv_out, *dP;     // [BH][N][d], [BH][N][d], [BH][N][dv], [H][d][m]
+  float *qp, *kp, *dqp, *dkp;       // workspace: [BH][N][m] each
+  float* dsum;                      // workspace: [BH][N] row sums <dO_i, O_i>
+  float* part;                      // workspace: [H][chunks][d][m] partial dP
+  int B, H, N, d, m, dv, causal, bf16;
+  int chunks;                       // row chunks of the dP reduction
+};
+int bwd_simt_chunks(int B, int N);
+cudaError_t launch_bwd_simt(const BwdSimtParams& p, cudaStream_t stream);
 
 // Single-query attention against the projected key cache, split over key chunks.
 constexpr int kDecodeMaxChunk = 8192;  // keys per chunk (scores in shared memory)

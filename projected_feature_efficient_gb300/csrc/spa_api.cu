@@ -407,12 +407,12 @@ int host_forward(const char* q, const char* k, const char* v, const char* P, flo
 // ---------------------------------------------------------------- fused backward
 // Workspace of the fused backward: the forward's prepared operands (so that
 // the recomputed scores are bit-identical to the forward's), bf16 Qp / Kp
-// tiles for the gradient products, the row statistics, the dQp accumulator,
-// the bf16 hi | lo rows of dQp and dKp, [P_h | P_h], the projection-gradient partial
-// R, and (when the caller has no log-sum-exp) lse plus a scratch output.
+// tiles for the gradient products, the row statistics, the fp32 dQp and dKp
+// accumulators (tile layout of bwd_common.cuh), and (when the caller has no
+// log-sum-exp) lse plus a scratch output.
 struct BwdLayout {
   Layout fwd;
-  size_t qb = 0, kb = 0, stats = 0, dqacc = 0, xq = 0, xk = 0, p2 = 0, R = 0;
+  size_t qb = 0, kb = 0, stats = 0, dqacc = 0, dkacc = 0;
   size_t lse = 0, out2 = 0, total = 0;
 };
 
@@ -430,14 +430,7 @@ BwdLayout make_bwd_layout(int B, int H, int N, int d, int m, int dv, bool own_ls
   L.kb = take(rows * m * 2);
   L.stats = take(rows * 4 * sizeof(float));
   L.dqacc = take(rows * m * sizeof(float));
-  L.xk = take(BH * N * 2 * m * 2);
-  // the library-GEMM finish also needs the split dQp rows, [P_h | P_h] and the
-  // dP partials; the one-pass finish reads dQp and P_h as they are
-  if (!spa::bwd_finish_tc_supported(d, m)) {
-    L.xq = take(BH * N * 2 * m * 2);
-    L.p2 = take(static_cast<size_t>(H) * d * 2 * m * 2);
-    L.R = take(static_cast<size_t>(H) * d * 2 * m * sizeof(float));
-  }
+  L.dkacc = take(rows * m * sizeof(float));
   if (own_lse) {
     L.lse = take(BH * N * sizeof(float));
     L.out2 = take(BH * N * dv * sizeof(float));
@@ -446,8 +439,10 @@ BwdLayout make_bwd_layout(int B, int H, int N, int d, int m, int dv, bool own_ls
   return L;
 }
 
-bool bwd_fused_eligible(int m, int dv, int dtype) {
-  return dtype == SPA_BF16 && spa::bwd_tc_supported(m, dv);
+// The tensor-core backward (fused kernel and one-pass finish); every other
+// shape runs on CUDA cores (run_backward_simt).
+bool bwd_fused_eligible(int d, int m, int dv, int dtype) {
+  return dtype == SPA_BF16 && spa::bwd_tc_supported(m, dv) && spa::bwd_finish_tc_supported(d, m);
 }
 
 // Fused backward, stage 1 on a workspace laid out by make_bwd_layout, after
@@ -494,7 +489,7 @@ int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int
   bp.Kb = reinterpret_cast<const uint16_t*>(w + L.kb);
   bp.stats = reinterpret_cast<const float*>(w + L.stats);
   bp.dqacc = reinterpret_cast<float*>(w + L.dqacc);
-  bp.xk = reinterpret_cast<uint16_t*>(w + L.xk);
+  bp.dkacc = reinterpret_cast<float*>(w + L.dkacc);
   bp.dv_out = dv;
   bp.BH = BH;
   bp.N = N;
@@ -510,45 +505,31 @@ int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int
   return cuda_status(spa::launch_bwd_tc(bp, stream));
 }
 
-// Fused backward, stage 3: dq, dk and dP from dQp and dKp.
+// Fused backward, stage 3: dq, dk and dP from dQp and dKp (one tensor-core pass).
 int bwd_stage_finish(const void* q, const void* k, const void* P, float* dq, float* dk, float* dP,
                      int B, int H, int N, int d, int m, int d_v, char* w, cudaStream_t stream) {
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
   const int BH = B * H;
   int st;
-  if (spa::bwd_finish_tc_supported(d, m)) {  // one tensor-core pass
-    spa::BwdFinishParams fp{};
-    if ((st = encode_bf16_rows(&fp.qmap, q, d, N, BH)) ||
-        (st = encode_bf16_rows(&fp.kmap, k, d, N, BH)) ||
-        (st = encode_bf16_rows(&fp.xkmap, w + L.xk, 2 * m, N, BH)) ||
-        (st = encode_rows_map(&fp.dqmap, dq, d, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
-        (st = encode_rows_map(&fp.dkmap, dk, d, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
-        (st = device_error_ptr(&fp.err)))
-      return st;
-    fp.dqacc = reinterpret_cast<const float*>(w + L.dqacc);
-    fp.P = static_cast<const __nv_bfloat16*>(P);
-    fp.dP = dP;
-    fp.B = B;
-    fp.H = H;
-    fp.N = N;
-    fp.NT = L.fwd.NT;
-    fp.d = d;
-    fp.m = m;
-    fp.limit_ns = kWaitLimitNs;
-    return cuda_status(spa::launch_bwd_finish_tc(fp, stream));
-  }
-  uint16_t* xq = reinterpret_cast<uint16_t*>(w + L.xq);
-  uint16_t* xk = reinterpret_cast<uint16_t*>(w + L.xk);
-  uint16_t* p2 = reinterpret_cast<uint16_t*>(w + L.p2);
-  if ((st = cuda_status(spa::launch_bwd_split(reinterpret_cast<const float*>(w + L.dqacc), xq, BH,
-                                              N, L.fwd.NT, m, stream))))
+  spa::BwdFinishParams fp{};
+  if ((st = encode_bf16_rows(&fp.qmap, q, d, N, BH)) ||
+      (st = encode_bf16_rows(&fp.kmap, k, d, N, BH)) ||
+      (st = encode_rows_map(&fp.dqmap, dq, d, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
+      (st = encode_rows_map(&fp.dkmap, dk, d, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
+      (st = device_error_ptr(&fp.err)))
     return st;
-  if ((st = cuda_status(
-           spa::launch_bwd_dup_p(static_cast<const __nv_bfloat16*>(P), p2, H, d, m, stream))))
-    return st;
-  const int rc = spa::run_backward_post(q, k, p2, xq, xk, reinterpret_cast<float*>(w + L.R), dq, dk,
-                                        dP, B, H, N, d, m, stream);
-  return rc ? SPA_ERR_CUDA : SPA_OK;
+  fp.dqacc = reinterpret_cast<const float*>(w + L.dqacc);
+  fp.dkacc = reinterpret_cast<const float*>(w + L.dkacc);
+  fp.P = static_cast<const __nv_bfloat16*>(P);
+  fp.dP = dP;
+  fp.B = B;
+  fp.H = H;
+  fp.N = N;
+  fp.NT = L.fwd.NT;
+  fp.d = d;
+  fp.m = m;
+  fp.limit_ns = kWaitLimitNs;
+  return cuda_status(spa::launch_bwd_finish_tc(fp, stream));
 }
 
 // The whole fused backward.  lse == NULL: the forward runs once more to
@@ -577,49 +558,100 @@ int check_bwd_staged(int B, int H, int N, int d, int m, int d_v, int dtype, cons
                      size_t ws_bytes) {
   int st = check_shape(B, H, N, d, m, d_v, dtype);
   if (st) return st;
-  if (d > 128 || !bwd_fused_eligible(m, d_v, dtype)) return SPA_ERR_UNSUPPORTED;
+  if (!bwd_fused_eligible(d, m, d_v, dtype)) return SPA_ERR_UNSUPPORTED;
   if (!ws) return SPA_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return SPA_ERR_ALIGN;
   if (ws_bytes < make_bwd_layout(B, H, N, d, m, d_v, false).total) return SPA_ERR_NOMEM;
   return SPA_OK;
 }
 
-// The materialised backward (fp32 inputs and the shapes the fused one does not cover).
-int run_backward_general(const void* q, const void* k, const void* v, const void* P,
-                         const float* out, const void* dO, float* dq, float* dk, float* dv,
-                         float* dP, int B, int H, int N, int d, int m, int d_v, int causal,
-                         int dtype, cudaStream_t s) {
-  spa::BwdParams bp{};
-  bp.q = q;
-  bp.k = k;
-  bp.v = v;
-  bp.P = P;
-  bp.dO = dO;
-  bp.out = out;
-  bp.dq = dq;
-  bp.dk = dk;
-  bp.dv_out = dv;
-  bp.dP = dP;
-  bp.B = B;
-  bp.H = H;
-  bp.N = N;
-  bp.d = d;
-  bp.m = m;
-  bp.dv = d_v;
-  bp.causal = causal != 0;
-  bp.bf16 = dtype == SPA_BF16;
-  // N x N blocks of as many heads as fit in 8 GB (at least one head)
-  bp.group = spa::backward_group(B, H, N, size_t(8) << 30);
-  const size_t bytes = spa::backward_workspace_bytes(bp);
-  void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPA_ERR_NOMEM;
+// The backward on CUDA cores (fp32 inputs and the shapes the tensor-core
+// kernels do not cover): flash-style, nothing N x N stored.  Workspace (from
+// the library's pool): Qp, Kp, dQp, dKp in fp32, the row sums <dO_i, O_i>, the
+// dP partials, and (without the caller's log-sum-exp) the forward's workspace,
+// a scratch output and lse.
+int run_backward_simt(const void* q, const void* k, const void* v, const void* P,
+                      const float* out, const float* lse, const void* dO, float* dq, float* dk,
+                      float* dv, float* dP, int B, int H, int N, int d, int m, int d_v, int causal,
+                      int dtype, cudaStream_t s) {
+  const size_t BH = static_cast<size_t>(B) * H, rows = BH * N;
+  const int chunks = spa::bwd_simt_chunks(B, N);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  const size_t oqp = take(rows * m * 4), okp = take(rows * m * 4), odq = take(rows * m * 4),
+               odk = take(rows * m * 4), ods = take(rows * 4),
+               opart = take(static_cast<size_t>(H) * chunks * d * m * 4);
+  size_t ofw = 0, oout = 0, olse = 0;
+  if (!lse) {
+    ofw = take(make_layout(B, H, N, m, dtype).total);
+    oout = take(rows * d_v * 4);
+    olse = take(rows * 4);
   }
-  const int rc = spa::run_backward(bp, ws, s);
-  const cudaError_t fe = cudaFreeAsync(ws, s);
-  if (rc) return SPA_ERR_CUDA;
-  return fe == cudaSuccess ? SPA_OK : SPA_ERR_CUDA;
+  char* w = nullptr;
+  if (int e = pool_alloc(reinterpret_cast<void**>(&w), o, s)) return e;
+  int st = SPA_OK;
+  if (!lse) {  // the forward once more, for its row log-sum-exp
+    st = run_prepare(q, k, P, B, H, N, d, m, dtype, w + ofw, s);
+    if (!st)
+      st = run_apply(v, reinterpret_cast<float*>(w + oout), B, H, N, m, d_v, causal, dtype, w + ofw,
+                     s, kWaitLimitNs, 0, reinterpret_cast<float*>(w + olse));
+    lse = reinterpret_cast<const float*>(w + olse);
+  }
+  if (!st) {  // Qp and Kp in fp32
+    spa::ProjParams pp{};
+    pp.x[0] = q;
+    pp.x[1] = k;
+    pp.P = P;
+    pp.out[0] = w + oqp;
+    pp.out[1] = w + okp;
+    pp.nx = 2;
+    pp.BH = B * H;
+    pp.H = H;
+    pp.N = N;
+    pp.d = d;
+    pp.m = m;
+    pp.NT = (N + spa::kTileRows - 1) / spa::kTileRows;
+    pp.bf16_in = dtype == SPA_BF16;
+    pp.mode = ProjOut::F32;
+    st = cuda_status(spa::launch_project(pp, s));
+  }
+  if (!st) {
+    spa::BwdSimtParams bp{};
+    bp.q = q;
+    bp.k = k;
+    bp.v = v;
+    bp.P = P;
+    bp.dO = dO;
+    bp.out = out;
+    bp.lse = lse;
+    bp.dq = dq;
+    bp.dk = dk;
+    bp.dv_out = dv;
+    bp.dP = dP;
+    bp.qp = reinterpret_cast<float*>(w + oqp);
+    bp.kp = reinterpret_cast<float*>(w + okp);
+    bp.dqp = reinterpret_cast<float*>(w + odq);
+    bp.dkp = reinterpret_cast<float*>(w + odk);
+    bp.dsum = reinterpret_cast<float*>(w + ods);
+    bp.part = reinterpret_cast<float*>(w + opart);
+    bp.B = B;
+    bp.H = H;
+    bp.N = N;
+    bp.d = d;
+    bp.m = m;
+    bp.dv = d_v;
+    bp.causal = causal != 0;
+    bp.bf16 = dtype == SPA_BF16;
+    bp.chunks = chunks;
+    st = cuda_status(spa::launch_bwd_simt(bp, s));
+  }
+  const cudaError_t fe = cudaFreeAsync(w, s);
+  if (st) return st;
+  return cuda_status(fe);
 }
 
 // Shared by both backward entry points; lse may be NULL.
@@ -639,13 +671,13 @@ int backward_entry(const void* q, const void* k, const void* v, const void* P, c
   if (st) return st;
   if (d > 128) return SPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !P || !out || !dO || !dq || !dk || !dv || !dP) return SPA_ERR_NULL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!bwd_fused_eligible(m, d_v, dtype))
-    return run_backward_general(q, k, v, P, out, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal,
-                                dtype, s);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(P) || !aligned16(dO) ||
       !aligned16(out) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dP))
     return SPA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!bwd_fused_eligible(d, m, d_v, dtype))
+    return run_backward_simt(q, k, v, P, out, lse, dO, dq, dk, dv, dP, B, H, N, d, m, d_v, causal,
+                             dtype, s);
   const size_t bytes = make_bwd_layout(B, H, N, d, m, d_v, lse == nullptr).total;
   void* ws = nullptr;
   if (int e = pool_alloc(&ws, bytes, s)) return e;
@@ -987,7 +1019,7 @@ int spa_attention_bwd_workspace_size(int B, int H, int N, int d, int m, int d_v,
     return SPA_OK;
   }
   if (st) return st;
-  if (d > 128 || !bwd_fused_eligible(m, d_v, dtype)) return SPA_ERR_UNSUPPORTED;
+  if (!bwd_fused_eligible(d, m, d_v, dtype)) return SPA_ERR_UNSUPPORTED;
   *bytes = make_bwd_layout(B, H, N, d, m, d_v, false).total;
   return SPA_OK;
 }

@@ -235,7 +235,9 @@ def test_backward_entry_points_validate_first(lib):
     assert bwd_lse(lib, dq=None) == NULL
     assert bwd_lse(lib, N=-3) == SHAPE
     assert bwd_lse(lib, d=192) == UNSUPPORTED     # d <= 128 for both backward versions
-    assert bwd_lse(lib, dO=A + 8) == ALIGN        # the fused path loads dO with TMA
+    assert bwd_lse(lib, dO=A + 8) == ALIGN        # the tensor-core path loads dO with TMA
+    assert bwd_lse(lib, dO=A + 8, m=128) == ALIGN  # the CUDA-core path checks the same
+    assert bwd_lse(lib, dO=A + 8, dtype=F32) == ALIGN
     assert bwd_lse(lib, N=0, dP=None) == NULL     # empty problem: dP is still zeroed
     # spa_attention_bwd (no lse) checks the same way
     assert lib.spa_attention_bwd(A, A, A, A, A, A, A, A, A, None, 1, 2, 256, 128, 32, 128, 1, BF16,
@@ -248,24 +250,22 @@ def bwd_ws_size(lib, B=1, H=2, N=256, d=128, m=32, dv=128, dtype=BF16):
     return st, n.value
 
 
-@pytest.mark.parametrize("m", [16, 32])
-def test_backward_workspace_size(lib, m):
-    st, small = bwd_ws_size(lib, N=256, m=m)
+@pytest.mark.parametrize("m,d", [(16, 128), (32, 128), (64, 128), (16, 64), (64, 64)])
+def test_backward_workspace_size(lib, m, d):
+    st, small = bwd_ws_size(lib, N=256, m=m, d=d)
     assert st == OK
-    st, big = bwd_ws_size(lib, N=4096, m=m)
+    st, big = bwd_ws_size(lib, N=4096, m=m, d=d)
     assert st == OK and big > small
-    # at least the forward's operands, the bf16 tiles, statistics, dQp
-    # accumulator and hi|lo rows of the problem (N = 4096, B*H = 2): dKp's,
-    # and dQp's too where the finish runs as library GEMMs (d = 128 here, so
-    # m = 32 takes the one-pass finish, which reads dQp as it is)
+    # at least the forward's operands, the bf16 Qp / Kp tiles, the statistics
+    # and the fp32 dQp and dKp accumulators of the problem (N = 4096, B*H = 2)
     rows = 2 * 4096
     KD = 3 * m if m == 16 else m
-    hilo_tensors = 1 if m == 32 else 2
-    assert big >= rows * (2 * 2 * KD + 4 + 2 * 2 * m + 16 + 4 * m + hilo_tensors * 2 * 2 * m)
+    assert big >= rows * (2 * 2 * KD + 4 + 2 * 2 * m + 16 + 2 * 4 * m)
 
 
 def test_backward_workspace_size_rejects(lib):
-    assert bwd_ws_size(lib, m=64)[0] == UNSUPPORTED   # outside the fused TMEM plan
+    assert bwd_ws_size(lib, m=128)[0] == UNSUPPORTED  # outside the fused TMEM plan
+    assert bwd_ws_size(lib, d=96)[0] == UNSUPPORTED   # the one-pass finish: d in {64, 128}
     assert bwd_ws_size(lib, dtype=F32)[0] == UNSUPPORTED
     assert bwd_ws_size(lib, dv=96)[0] == UNSUPPORTED
     assert bwd_ws_size(lib, N=0) == (OK, 0)
@@ -279,7 +279,7 @@ def test_backward_stages_check_their_workspace(lib):
     assert prep(None, need) == NULL
     assert prep(A + 16, need) == ALIGN      # 256-byte alignment for the workspace
     assert prep(A, need - 1) == NOMEM
-    assert prep(A, need, m=64) == UNSUPPORTED
+    assert prep(A, need, m=128) == UNSUPPORTED
     app = lambda ws, nb: lib.spa_attention_bwd_apply(A, A, A, 1, 2, 256, 128, 32, 128, 1, BF16,
                                                      ws, nb, None)
     assert app(None, need) == NULL

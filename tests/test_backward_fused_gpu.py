@@ -77,13 +77,20 @@ FUSED_SHAPES = [
     (2, 2, 257, 128, 32, 128, True),    # three tiles, ragged, causal
     (1, 2, 300, 128, 16, 128, True),    # m = 16: split-bf16 scores
     (1, 3, 384, 64, 32, 128, False),    # whole tiles
-    (2, 1, 129, 96, 16, 64, False),     # d = 96, d_v = 64
+    (2, 1, 129, 96, 16, 64, False),     # d = 96, d_v = 64: the CUDA-core backward
     (4, 16, 512, 64, 32, 64, True),     # 256 items: several per CTA
     (2, 40, 256, 64, 16, 128, False),   # 160 items, non-causal order
-    # d = 128, m = 32: the projection gradients in one tensor-core pass
+    # the projection gradients in one tensor-core pass
     (1, 3, 50, 128, 32, 128, True),     # one partial tile per (side, b, h)
     (3, 5, 700, 128, 32, 64, False),    # dP_h summed over three batch entries, ragged
     (2, 24, 1024, 128, 32, 128, True),  # 768 units: CTA ranges cross heads
+    (2, 3, 333, 64, 16, 64, True),      # d = 64 (zero half of X^T), m = 16 (padded G rows)
+    # m = 64: P^T over S^T in tensor memory at d_v = 128, single-buffered Qp
+    # tiles, dQp in four 16-column slabs
+    (1, 2, 300, 128, 64, 128, True),
+    (2, 2, 257, 64, 64, 128, False),
+    (1, 3, 200, 128, 64, 64, True),     # d_v = 64: P^T in columns of its own
+    (1, 6, 1100, 128, 64, 128, True),   # several items per CTA, ragged
 ]
 
 
@@ -147,11 +154,14 @@ def test_fused_backward_full_size_sampled_heads():
             f"{name}: rel-F {rel_f:.2e}, rel-max {rel_max:.2e}"
 
 
-def test_materialised_path_still_serves_m64():
-    """m = 64 is outside the fused kernel's tensor-memory plan: the general
-    backward answers, and agrees with the oracle."""
+@pytest.mark.parametrize("m,dv", [(128, 128), (128, 64)])
+def test_cuda_core_backward_serves_m128(m, dv):
+    """m = 128 does not fit the fused kernel's tensor memory: the CUDA-core
+    backward (flash-style, nothing N x N stored) answers, and agrees with the
+    oracle; with and without the forward's log-sum-exp it gives the same bits
+    for dk and dv."""
     pkg = spa()
-    q, k, v, P, dO = _problem(1, 2, 150, 64, 64, 64, True, "bf16", seed=55)
+    q, k, v, P, dO = _problem(1, 2, 150, 128, m, dv, True, "bf16", seed=55)
     q_, k_, v_, P_, dO_ = (t.cuda() for t in (q, k, v, P, dO))
     out, lse = pkg.spa_attention_fwd_lse(q_, k_, v_, P_, causal=True)
     got = pkg.spa_attention_bwd_lse(q_, k_, v_, P_, out, lse, dO_, causal=True)
@@ -159,3 +169,30 @@ def test_materialised_path_still_serves_m64():
     for name, gg, rr in zip(("dq", "dk", "dv", "dP"), got, ref):
         rel_f, rel_max = rel_errors(gg.cpu().numpy(), rr)
         assert rel_f <= REL_F and rel_max <= 2 * REL_F, f"{name}: {rel_f:.2e} {rel_max:.2e}"
+    again = pkg.spa_attention_bwd(q_, k_, v_, P_, out, dO_, causal=True)
+    for a, b in zip(got, again):
+        assert torch.equal(a, b)
+
+
+def test_staged_backward_gives_the_entry_points_bits_m64():
+    """prepare + apply + finish on a caller workspace gives the allocating
+    entry point's dk and dv bit for bit at m = 64 (dq, dP within reduce-add
+    order)."""
+    pkg = spa()
+    B, H, N, d, m, dv = 2, 3, 400, 128, 64, 128
+    q, k, v, P, dO = (t.cuda() for t in _problem(B, H, N, d, m, dv, True, "bf16", seed=66))
+    out, lse = pkg.spa_attention_fwd_lse(q, k, v, P, causal=True)
+    want = pkg.spa_attention_bwd_lse(q, k, v, P, out, lse, dO, causal=True)
+    ws = torch.empty(pkg.spa_attention_bwd_workspace_size(B, H, N, d, m, dv, pkg.SPA_BF16),
+                     dtype=torch.uint8, device="cuda")
+    dq = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+    dk, dvo = torch.empty_like(dq), torch.empty((B, H, N, dv), dtype=torch.float32, device="cuda")
+    dP = torch.empty((H, d, m), dtype=torch.float32, device="cuda")
+    pkg.spa_attention_bwd_prepare(q, k, P, out, lse, dO, ws)
+    pkg.spa_attention_bwd_apply(v, dO, dvo, ws, B, H, N, d, m, causal=True)
+    pkg.spa_attention_bwd_finish(q, k, P, dq, dk, dP, dv, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, want[1]) and torch.equal(dvo, want[2])
+    for a, b in ((dq, want[0]), (dP, want[3])):
+        assert torch.allclose(a, b, rtol=1e-4, atol=1e-5 * float(b.abs().max()))
+    assert pkg.device_error() == 0

@@ -1,9 +1,11 @@
-"""Gradients on the GPU against the oracle's (pinned) gradients.
+"""Gradients on the GPU against the oracle's (pinned) gradients, through
+spa_attention_bwd (the forward run once more for its log-sum-exp).
 
-Tolerance, from the arithmetic: bf16 inputs go through TF32 products with fp32
-accumulation; every value is exact in TF32 except the fp32 intermediates (Qp,
-A, dS, ...), each rounded to 11 significant bits once per product stage, so
-a few stages stay well inside rel-F 1e-2.  fp32 inputs use fp32 products:
+Tolerance, from the arithmetic: bf16 shapes of the tensor-core backward round
+the probabilities and dS once to bf16 for their products (fp32 accumulation),
+a few 2^-9 roundings per term: rel-F 1e-2.  fp32 inputs (and the other
+shapes) take the CUDA-core backward, fp32 arithmetic throughout, whose
+rounding errors grow with the sums' lengths (N, m, d_v of a few hundred):
 rel-F 1e-4.  max |err| is bounded relative to the tensor's largest entry."""
 import numpy as np
 import pytest
