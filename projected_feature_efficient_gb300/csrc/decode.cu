@@ -11,9 +11,9 @@
 // The cache rows themselves are written by the projection kernels (project.cu,
 // output mode F16ROWS).
 //
-//   decode_qproj_kernel   q~ = q P_h (fp32) once per (batch, head).
 //   decode_kernel         one query per (batch, head) against keys 0 .. L-1,
-//                         split over key chunks: scores
+//                         split over key chunks: q~ = q P_h (fp32, in every
+//                         CTA from L2), scores
 //                         from the fp16 cache in fp32, chunk max and sum, and
 //                         the chunk's P V in fp32; writes (max, sum, O) per
 //                         chunk.  HBM-bound: per key 2m + 4 bytes of cache and
@@ -32,31 +32,39 @@ namespace {
 // ------------------------------------------------------------ decode
 constexpr int kDecodeThreads = 256;
 
-// q~ = q P_h * log2(e)/sqrt(m), once per (batch, head): grid BH, m threads.
-__global__ void __launch_bounds__(128) decode_qproj_kernel(const DecodeParams p) {
-  const int bh = blockIdx.x, h = bh % p.H, k = threadIdx.x;
-  if (k >= p.m) return;
-  const __nv_bfloat16* q = p.q + static_cast<size_t>(bh) * p.d;
-  const __nv_bfloat16* P = p.P + static_cast<size_t>(h) * p.d * p.m + k;
-  float acc = 0.f;
-  for (int l = 0; l < p.d; ++l) acc = fmaf(__bfloat162float(q[l]), __bfloat162float(P[l * p.m]), acc);
-  p.qproj[static_cast<size_t>(bh) * p.m + k] = acc * p.qscale;
-}
-
 // grid (nsplit, BH), 256 threads.  Chunk c covers keys [c*chunk, min(L, (c+1)*chunk)).
 template <int DV>
 __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeParams p) {
   extern __shared__ float sc[];  // scores, then probabilities, of this chunk
   __shared__ float qs[128];      // q~ * log2(e)/sqrt(m)
+  __shared__ float qpart[kDecodeThreads];
   __shared__ float red[kDecodeThreads / 32];
   __shared__ float oacc[kDecodeThreads / 32][DV];
   const int bh = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = split * p.chunk, n = min(p.L, k0 + p.chunk) - k0;
 
-  // q~ (projected and scaled once per (batch, head) by decode_qproj_kernel)
-  for (int k = tid; k < p.m; k += kDecodeThreads) qs[k] = p.qproj[static_cast<size_t>(bh) * p.m + k];
-  __syncthreads();
+  // q~ = q P_h * log2(e)/sqrt(m), by every CTA of the (batch, head) (8 KB of
+  // P_h from L2 at m = 32; a separate launch cost more than the work): thread
+  // t sums column t % m over the rows l = t / m (mod G), coalesced across the
+  // columns, and the G partial sums meet in shared memory
+  {
+    const int G = kDecodeThreads / p.m;  // row groups (m divides 256)
+    const int k = tid % p.m, g = tid / p.m;
+    const __nv_bfloat16* q = p.q + static_cast<size_t>(bh) * p.d;
+    const __nv_bfloat16* P = p.P + static_cast<size_t>(bh % p.H) * p.d * p.m + k;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int l = g; l < p.d; l += G) acc = fmaf(__bfloat162float(q[l]), __bfloat162float(P[l * p.m]), acc);
+    qpart[tid] = acc;
+    __syncthreads();
+    if (tid < p.m) {
+      float s = 0.f;
+      for (int gg = 0; gg < G; ++gg) s += qpart[gg * p.m + tid];
+      qs[tid] = s * p.qscale;
+    }
+    __syncthreads();
+  }
 
   // scores in log2 units: one key row per thread, m fp16 values in 16-byte pieces
   const uint16_t* kc = p.kc + (static_cast<size_t>(bh) * p.cap + k0) * p.m;
@@ -157,20 +165,46 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodePara
   }
 }
 
-// grid BH, DV threads: out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c
+// grid BH, 256 threads: out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+// The chunk maxima are reduced by the whole block; then 256 / DV groups of
+// DV threads (one per output column) take every (256 / DV)-th chunk, with the
+// loads of several chunks in flight, and meet in shared memory.
 template <int DV>
-__global__ void __launch_bounds__(DV) decode_combine_kernel(const DecodeParams p) {
-  const int bh = blockIdx.x, c = threadIdx.x;
+__global__ void __launch_bounds__(kDecodeThreads) decode_combine_kernel(const DecodeParams p) {
+  constexpr int G = kDecodeThreads / DV;
+  __shared__ float red[kDecodeThreads / 32];
+  __shared__ float acc_o[G][DV], acc_l[G];
+  const int bh = blockIdx.x, tid = threadIdx.x, c = tid % DV, g = tid / DV;
   const float* part = p.part + static_cast<size_t>(bh) * p.nsplit * (2 + DV);
   float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, part[s * (2 + DV)]);
+  for (int s = tid; s < p.nsplit; s += kDecodeThreads) M = fmaxf(M, part[s * (2 + DV)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if ((tid & 31) == 0) red[tid >> 5] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < kDecodeThreads / 32; ++w) M = fmaxf(M, red[w]);
   float l = 0.f, o = 0.f;
-  for (int s = 0; s < p.nsplit; ++s) {
-    const float w = exp2f(part[s * (2 + DV)] - M);
-    l = fmaf(w, part[s * (2 + DV) + 1], l);
-    o = fmaf(w, part[s * (2 + DV) + 2 + c], o);
+#pragma unroll 4
+  for (int s = g; s < p.nsplit; s += G) {
+    const float* ps = part + s * (2 + DV);
+    const float w = exp2f(ps[0] - M);
+    l = fmaf(w, ps[1], l);
+    o = fmaf(w, ps[2 + c], o);
   }
-  p.out[static_cast<size_t>(bh) * DV + c] = o / l;
+  acc_o[g][c] = o;
+  if (c == 0) acc_l[g] = l;
+  __syncthreads();
+  if (g == 0) {
+    float os = 0.f, ls = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      os += acc_o[gg][c];
+      ls += acc_l[gg];
+    }
+    p.out[static_cast<size_t>(bh) * DV + c] = os / ls;
+  }
 }
 
 }  // namespace
@@ -194,22 +228,20 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(p.chunk) * sizeof(float);
   dim3 grid(p.nsplit, p.BH);
   cudaError_t e;
-  decode_qproj_kernel<<<p.BH, 128, 0, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.dv == 128) {
     e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     decode_kernel<128><<<grid, kDecodeThreads, smem, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    decode_combine_kernel<128><<<p.BH, 128, 0, stream>>>(p);
+    decode_combine_kernel<128><<<p.BH, kDecodeThreads, 0, stream>>>(p);
   } else if (p.dv == 64) {
     e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     decode_kernel<64><<<grid, kDecodeThreads, smem, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    decode_combine_kernel<64><<<p.BH, 64, 0, stream>>>(p);
+    decode_combine_kernel<64><<<p.BH, kDecodeThreads, 0, stream>>>(p);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -169,7 +169,6 @@ struct DecodeParams {
   const __nv_bfloat16* v;  // [BH][cap][dv]
   float* out;              // [BH][dv]
   float* part;             // [BH][nsplit][2 + dv] chunk results (workspace)
-  float* qproj;            // [BH][m] q~ scaled by qscale (workspace)
   int BH, H, L, d, m, dv, cap, nsplit, chunk;
   float qscale;            // log2(e)/sqrt(m)
 };

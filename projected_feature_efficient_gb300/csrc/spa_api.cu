@@ -893,19 +893,16 @@ int spa_attention_decode(const void* q, const void* P, const void* kc, const flo
   dp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m)));
   spa::decode_split(dp.BH, L, sms, &dp.nsplit, &dp.chunk);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t part = align256(static_cast<size_t>(dp.BH) * dp.nsplit * (2 + d_v) * sizeof(float));
-  const size_t qpb = static_cast<size_t>(dp.BH) * m * sizeof(float);
+  const size_t part = static_cast<size_t>(dp.BH) * dp.nsplit * (2 + d_v) * sizeof(float);
   // from the library's own pool, which keeps what it has reserved: a decode loop
   // synchronises every step, and the default pool would hand the scratch back
   // to the driver at each synchronisation and reserve it again on the next call
   cudaMemPool_t pool = nullptr;
   if (host_pool(&pool) != SPA_OK) return SPA_ERR_CUDA;
-  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dp.part), part + qpb, pool, s) !=
-      cudaSuccess) {
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dp.part), part, pool, s) != cudaSuccess) {
     cudaGetLastError();
     return SPA_ERR_NOMEM;
   }
-  dp.qproj = reinterpret_cast<float*>(reinterpret_cast<char*>(dp.part) + part);
   const int st = cuda_status(spa::launch_decode(dp, s));
   const cudaError_t fe = cudaFreeAsync(dp.part, s);
   if (st) return st;
