@@ -517,6 +517,19 @@ def measure_forward(args, w, rank, world, dev, dist):
     return line
 
 
+def repeats_for(fn, steps, min_seconds, stream, cap=100000):
+    """Repeats per step so that `steps` steps of `fn` last at least min_seconds
+    (one pass of fn timed with CUDA events after the warm-up)."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = max(e0.elapsed_time(e1) * 1e-3, 1e-7)
+    return int(max(1, min(cap, math.ceil(min_seconds / (steps * t)))))
+
+
 def results_done(path, key, src_hash):
     """True if the results file already holds the line of `key` measured on the
     current kernel source (a sweep resumes where it stopped)."""
@@ -643,20 +656,22 @@ def run_decode(args, rank, world, local_rank):
         spa.spa_attention_decode(q, P, kc, kmul, v, L, out=out)
     barrier()
     K = args.steps
+    R = repeats_for(lambda: spa.spa_attention_decode(q, P, kc, kmul, v, L, out=out), K,
+                    args.min_seconds, stream)
     sampler = ClockSampler(physical_device(local_rank))
     time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     barrier()
     sampler.mark_start()
     ev[0].record(stream)
-    for _ in range(K):
+    for _ in range(K * R):
         spa.spa_attention_decode(q, P, kc, kmul, v, L, out=out)
     ev[1].record(stream)
     barrier()
     sampler.mark_end()
     clocks = sampler.summary()
     sampler.stop()
-    t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
+    t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev) / R  # per K decode steps
     nbytes = decode_bytes(B, H, L, m, dv)
     value = world * nbytes * K / (t_ms * 1e-3) / 1e9
 
@@ -681,7 +696,7 @@ def run_decode(args, rank, world, local_rank):
         achieved = nbytes / (t_ms / K * 1e-3) / 1e9
         line = {
             "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": t_ms / K,
+            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": t_ms * R / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"D1{'' if B == 8 else '-subset'}: decode, B={B} H={H} cached keys L={L} d={d} m={m} "
@@ -690,6 +705,7 @@ def run_decode(args, rank, world, local_rank):
                        "bytes_per_key": 2 * m + 4 + 2 * dv,
                        "bytes_per_key_k_v_cache": 2 * d + 2 * dv,
                        "l2": f"cache and values ({nbytes / 1e9:.2f} GB) larger than L2; no flush",
+                       "repeats_per_step": R,
                        "api": "spa_attention_decode on a resident cache",
                        "parallelism": f"dp{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm[0], "unit": "GB/s",
@@ -703,7 +719,7 @@ def run_decode(args, rank, world, local_rank):
                     "steps": Ke},
             "cache_append": {"ms": append_ms, "GB/s": B * H * L * (2 * d + 2 * m + 4) / append_ms / 1e6,
                              "api": "spa_kcache_append of all L keys (prefill)"},
-            "gpu_launches": 2 * K,
+            "gpu_launches": 2 * K * R,
             "clocks": clocks,
         }
         if cpu is not None:
@@ -780,13 +796,14 @@ def run_backward(args, rank, world, local_rank):
         step()
     barrier()
     K = args.steps
+    R = repeats_for(step, K, args.min_seconds, stream)
     sampler = ClockSampler(physical_device(local_rank))
     time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     barrier()
     sampler.mark_start()
     ev[0].record(stream)
-    for _ in range(K):
+    for _ in range(K * R):
         step()
     ev[1].record(stream)
     barrier()
@@ -802,7 +819,7 @@ def run_backward(args, rank, world, local_rank):
     t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
     k_ms = ev[2].elapsed_time(ev[3]) / K
     fl = bwd_flops(B, H, N, d, m, dv, w.causal)
-    value = world * fl * K / (t_ms * 1e-3) / 1e12
+    value = world * fl * K * R / (t_ms * 1e-3) / 1e12
     if spa.device_error() != 0:
         raise RuntimeError("a kernel gave up on a bounded wait")
     cpu = None
@@ -826,7 +843,8 @@ def run_backward(args, rank, world, local_rank):
         achieved = bwd_kernel_flops(B, H, N, m, dv, w.causal) / (k_ms * 1e-3) / 1e12
         line = {
             "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": W, "ms_per_step": t_ms / K, "higher_is_better": True,
+            "warmup": W, "ms_per_step": t_ms / K, "ms_per_backward": t_ms / (K * R),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{w.name} backward: B={B} H={H} N={N} d={d} m={m} d_v={dv} "
                                    f"bf16 {'causal' if w.causal else 'non-causal'}; upstream "
@@ -835,16 +853,17 @@ def run_backward(args, rank, world, local_rank):
                        "api": "spa_attention_bwd_prepare / _apply / _finish (forward output "
                               "and lse computed once, outside)",
                        "l2": "inputs and workspace (q, k, v, dO and the workspace) exceed L2",
+                       "repeats_per_step": R,
                        "parallelism": f"dp{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                          "kernel": "bwd_ws_kernel (S, dP, dV, dKp, dQp on tcgen05)",
                          "peak_source": f"{peak_src} bf16 burst",
                          "frac_of_sustained": achieved / peak_sus},
-            "kernels_ms_per_step": {"bwd_ws_kernel": k_ms, "rest": t_ms / K - k_ms},
-            # ours per step: projection, statistics, the kernel, the finish
+            "kernels_ms_per_backward": {"bwd_ws_kernel": k_ms, "rest": t_ms / (K * R) - k_ms},
+            # ours per backward: projection, statistics, the kernel, the finish
             # (plus two memsets)
-            "gpu_launches": 4 * K,
+            "gpu_launches": 4 * K * R,
             "clocks": clocks,
         }
         if cpu is not None:
@@ -904,13 +923,15 @@ def run_sfa(args, rank, world, local_rank):
         spa.spa_topk_features(q, topk, out=ysel)
     barrier()
     K = args.steps
+    R = repeats_for(lambda: spa.spa_sfa_attention_fwd(q, k, v, topk, out=out), K,
+                    args.min_seconds, stream)
     sampler = ClockSampler(physical_device(local_rank))
     time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     barrier()
     sampler.mark_start()
     ev[0].record(stream)
-    for _ in range(K):
+    for _ in range(K * R):
         spa.spa_sfa_attention_fwd(q, k, v, topk, out=out)
     ev[1].record(stream)
     for _ in range(K):
@@ -923,7 +944,7 @@ def run_sfa(args, rank, world, local_rank):
     t_ms = max_over_ranks(ev[0].elapsed_time(ev[1]), dist, dev)
     tk_ms = ev[1].elapsed_time(ev[2]) / K
     fl = sfa_flops(B, H, N, d, dv, w.causal)
-    value = world * fl * K / (t_ms * 1e-3) / 1e12
+    value = world * fl * K * R / (t_ms * 1e-3) / 1e12
     if spa.device_error() != 0:
         raise RuntimeError("a kernel gave up on a bounded wait")
     cpu = None
@@ -952,11 +973,13 @@ def run_sfa(args, rank, world, local_rank):
         tk_gbs = 2.0 * q.numel() * 2 / (tk_ms * 1e-3) / 1e9
         line = {
             "metric": SFA_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": W, "ms_per_step": t_ms / K, "higher_is_better": True, "scaling": "weak",
+            "warmup": W, "ms_per_step": t_ms / K, "ms_per_forward": t_ms / (K * R),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"SFA on the C4 shape: B={B} H={H} N={N} d={d} d_v={dv} "
                                    f"bf16, Top-k k={topk} of q and k rows, full attention",
                        "api": "spa_sfa_attention_fwd", "l2": "inputs (805 MB) exceed L2",
+                       "repeats_per_step": R,
                        "parallelism": f"dp{world}"},
             "roofline": {"bound": "hbm", "achieved": tk_gbs, "peak": hbm[0], "unit": "GB/s",
                          "frac": tk_gbs / hbm[0],
@@ -964,8 +987,8 @@ def run_sfa(args, rank, world, local_rank):
                                                       sources=TOPK_SOURCES) if H == 32 else None),
                          "kernel": "topk_rows_bf16_tma_kernel (reads and writes q: 2 x 2 bytes per value)",
                          "peak_source": hbm[1]},
-            "kernels_ms_per_step": {"topk_q": tk_ms, "rest": t_ms / K - tk_ms},
-            "gpu_launches": 5 * K,  # Top-k of q and k, P = I, projection, attention
+            "kernels_ms_per_forward": {"topk_q": tk_ms, "rest": t_ms / (K * R) - tk_ms},
+            "gpu_launches": 5 * K * R,  # Top-k of q and k, P = I, projection, attention
             "clocks": clocks,
         }
         if cpu is not None:
