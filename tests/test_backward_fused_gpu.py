@@ -154,6 +154,34 @@ def test_fused_backward_full_size_sampled_heads():
             f"{name}: rel-F {rel_f:.2e}, rel-max {rel_max:.2e}"
 
 
+def test_fused_backward_c4_m64_full_size_sampled_head():
+    """The C4 backward at m = 64 (B=1 H=32 N=32768 d=128 d_v=128, non-causal),
+    the shape and launch bench.py --backward --config C4 --m 64 times, on the
+    GPU, checked against the oracle on one head (B = 1, so dP_h is that
+    head's alone).  The oracle's gradients of one full head take about a
+    minute on the host cores."""
+    pkg = spa()
+    w = si.WORKLOADS["C4"].with_m(64)
+    q, k, v = si.make_qkv(w, seed=94)
+    P = si.make_P(w, seed=95)
+    g = torch.Generator().manual_seed(96)
+    dO = torch.randn((w.B, w.H, w.N, w.dv), generator=g, dtype=torch.float64).to(w.torch_dtype)
+    q_, k_, v_, P_, dO_ = (t.cuda() for t in (q, k, v, P, dO))
+    out, lse = pkg.spa_attention_fwd_lse(q_, k_, v_, P_, causal=False)
+    dq, dk, dv, dP = pkg.spa_attention_bwd_lse(q_, k_, v_, P_, out, lse, dO_, causal=False)
+    torch.cuda.synchronize()
+    h = 19
+    sl = slice(h, h + 1)
+    ref = oracle.attention_bwd(q[:, sl].contiguous(), k[:, sl].contiguous(), v[:, sl].contiguous(),
+                               P[sl].contiguous(), dO[:, sl].contiguous(), causal=False)
+    for name, gg, rr in zip(("dq", "dk", "dv", "dP"),
+                            (dq[:, sl], dk[:, sl], dv[:, sl], dP[sl]), ref):
+        rel_f, rel_max = rel_errors(gg.cpu().numpy(), rr)
+        assert rel_f <= REL_F and rel_max <= 2 * REL_F, \
+            f"{name}: rel-F {rel_f:.2e}, rel-max {rel_max:.2e}"
+    assert pkg.device_error() == 0
+
+
 @pytest.mark.parametrize("m,dv", [(128, 128), (128, 64)])
 def test_cuda_core_backward_serves_m128(m, dv):
     """m = 128 does not fit the fused kernel's tensor memory: the CUDA-core
