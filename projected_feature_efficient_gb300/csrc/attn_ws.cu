@@ -3,15 +3,16 @@
 //
 // Persistent: one CTA per SM walks a static list of work items, each a pair
 // of 128-row query tiles (t = 0, 1) of one (batch, head), streaming the
-// key/value tiles of that head once for both query tiles.  Twelve warps in
-// three warpgroups (setmaxnreg moves registers from the third to the first two):
-//   warps 0-3  softmax and output for query tile 0   (TMEM lanes 0-127 of S0 / O0)
-//   warps 4-7  softmax and output for query tile 1   (TMEM lanes 0-127 of S1 / O1)
-//   warp  8    loads: per item the two Qp tiles, then a ring of STAGES slots,
-//              each a Kp tile (one bulk copy) and a V tile (TMA, 128-byte
-//              swizzle) completing on one barrier
-//   warp  9    tensor-memory allocation and tcgen05.mma issue
-//   warps 10-11 idle (they complete the control warpgroup for the register split)
+// key/value tiles of that head once for both query tiles.  Sixteen warps in
+// four warpgroups (setmaxnreg moves registers from the last two to the first two):
+//   warps 0-3   softmax for query tile 0   (TMEM lanes 0-127 of S0)
+//   warps 4-7   softmax for query tile 1   (TMEM lanes 0-127 of S1)
+//   warps 8-11  output: O_t / l for both tiles (TMEM lanes 0-127 of O0 / O1)
+//   warp  12    loads: per item the two Qp tiles, then a ring of STAGES slots,
+//               each a Kp tile (one bulk copy) and a V tile (TMA, 128-byte
+//               swizzle) completing on one barrier
+//   warp  13    tensor-memory allocation and tcgen05.mma issue
+//   warps 14-15 idle (they complete the control warpgroup for the register split)
 // Tensor memory (512 columns):  S0 | S1 | O0 | O1, with the bf16 probabilities
 // P_t written over the first 64 columns of S_t and read from there by the PV
 // product.  The MMA issue order per key tile j is
@@ -29,12 +30,16 @@
 // starts at ring slot 0; every slot keeps its own phase bit).
 //
 // Between items nothing drains: the loader refills the Q tiles as soon as the
-// last score MMA of the item has completed (q_empty), the next item's first
-// score MMAs follow the last PV MMAs in the same issue stream, and each
-// softmax warpgroup writes its finished O_t (o_final[t]) through a small
-// shared-memory staging buffer with TMA stores while the next item's first
-// scores are computed; the next PV_t(0), which overwrites O_t, waits for
-// o_empty[t].
+// last score MMA of the item has completed (q_empty), and the next item's
+// first score MMAs follow the last PV MMAs in the same issue stream.  A
+// softmax warpgroup hands its rows' max and sum to the output warpgroup
+// through shared memory (stats_full[t]) and goes straight on to the next
+// item's scores; the output warpgroup writes the finished O_t (o_final[t])
+// through a small shared-memory staging buffer with TMA stores, and the next
+// PV_t(0), which overwrites O_t, waits for o_empty[t].  (With the output on
+// the softmax warpgroups, each item boundary cost them the output step:
+// moving it to its own warpgroup gave C3 +2.5%, C4 m = 32 +1.6%, m = 64
+// +3.3%, C5 +2.0%, bit-identical.)
 //
 // Online softmax (base 2, log2(e)/sqrt(m) already folded into Qp): the
 // running max only moves when a tile's max exceeds it by more than 20; in
@@ -42,7 +47,7 @@
 // same relative precision), which leaves the final O / l unchanged up to
 // rounding and skips almost every rescale of O.
 //
-// With an `lse` buffer the output step also writes each row's log-sum-exp
+// With an `lse` buffer the output warpgroup also writes each row's log-sum-exp
 // (m + log2 l, converted to natural log), which the fused backward uses to
 // recompute the probabilities.
 //
@@ -61,26 +66,42 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;  // three warpgroups
-// Register split.  The block is launched with 384 x 168 = 64512 registers; the
-// control warpgroup (warps 8-11) gives up part of its share to the two
-// softmax warpgroups, 184 each.  The control warpgroup keeps 128
-// (128 * (184 + 184 + 128) = 63488), or 136 (= 64512) where the deeper score
-// GEMM's unrolled issue needs more.  Each warpgroup executes its setmaxnreg
-// once, at the top of its branch.
-template <int KD>
+constexpr int kThreads = 512;  // four warpgroups
+// Register split.  The block is launched with 512 x 128 = 65536 registers; the
+// output and control warpgroups give up part of their share to the two
+// softmax warpgroups, 184 each, and keep 72 each
+// (128 * (184 + 184 + 72 + 72) = 65536).  The issuer stays within 72 because
+// its descriptor arithmetic is done at each MMA (opaque64/opaque32 below)
+// instead of being hoisted out of the item loop.  Each warpgroup executes its
+// setmaxnreg once, at the top of its branch.
 struct RegSplit {
   static constexpr uint32_t kSoftmax = 184;
-  static constexpr uint32_t kControl = KD >= 64 ? 136 : 128;
-  static_assert(128 * (2 * kSoftmax + kControl) <= 384 * 168, "register split exceeds the launch");
+  static constexpr uint32_t kOutput = 72;
+  static constexpr uint32_t kControl = 72;
+  static_assert(128 * (2 * kSoftmax + kOutput + kControl) <= kThreads * 128,
+                "register split exceeds the launch");
 };
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr uint32_t kOutBar = 3;  // named barrier of the output warpgroup
+// A value the compiler must treat as new at each use, so that descriptor
+// arithmetic is done where the MMA is issued instead of being hoisted out of
+// the item loop into registers.
+__device__ __forceinline__ uint64_t opaque64(uint64_t x) {
+  uint64_t r;
+  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t opaque32(uint32_t x) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
 constexpr float kRescaleThreshold = 20.f;  // log2 units: p <= 2^20 between rescales
 constexpr float kSumLimit = 1048576.f;     // 2^20: a tile row sum within it bounds every p
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr int kBoxBytes = kTileRows * 128;  // one 128-row x 128-byte output box
-constexpr int kMaxDynSmem = 227 * 1024 - 1024;  // per-block limit less the static part
+constexpr int kMaxDynSmem = 227 * 1024 - 5 * 1024;  // per-block limit less the static part
 
 template <int KD, int DV>
 struct WsPlan {
@@ -92,10 +113,12 @@ struct WsPlan {
   static constexpr int kK = 2 * kQBytes;
   static constexpr int kV = kK + kStages * kKBytes;
   static constexpr int kOps = kV + kStages * kVBytes;   // end of the operand area
-  // output staging: per query tile, 1 or 2 boxes of 32 fp32 columns x 128 rows
-  static constexpr int kBoxesPerTile = kOps + 1024 + 4 * kBoxBytes <= kMaxDynSmem ? 2 : 1;
+  // output staging: 4, 2 or 1 boxes of 32 fp32 columns x 128 rows
+  static constexpr int kBoxes = kOps + 1024 + 4 * kBoxBytes <= kMaxDynSmem   ? 4
+                                : kOps + 1024 + 2 * kBoxBytes <= kMaxDynSmem ? 2
+                                                                              : 1;
   static constexpr int kStage = kOps;
-  static constexpr int kBytes = kStage + 2 * kBoxesPerTile * kBoxBytes;
+  static constexpr int kBytes = kStage + kBoxes * kBoxBytes;
   // one CTA per SM: a second one would wait in tcgen05.alloc for the 512 columns
   static constexpr int kLaunch = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
   static_assert(kLaunch <= kMaxDynSmem, "shared-memory plan too large");
@@ -107,6 +130,7 @@ struct Bars {
   uint64_t kv_full[3], kv_empty[3];
   uint64_t s_full[2], p_full[2];
   uint64_t o_final[2], o_empty[2];
+  uint64_t stats_full[2];
   uint64_t drain;
 };
 
@@ -185,16 +209,17 @@ __device__ __forceinline__ void run_loader(const AttnTcParams& p, const CUtensor
 }
 
 // ---------------------------------------------------------------- output
-// One softmax warpgroup writes its finished O_t / l (fp32) for query tile qt:
+// The output warpgroup writes a finished O_t / l (fp32) for query tile qt:
 // DV/32 boxes of 128 rows x 128 B, staged in the 128-byte swizzle of the
 // output tensor map (16-byte chunk q of row r sits at chunk q ^ (r % 8), which
 // also spreads a warp's stores over all banks) through kBuffers box buffers
-// at `stage`, each written out by a TMA tile store that clips rows past N.
-// The warps arrive on o_empty once their last read of O_t is done.
+// at `stage` (box buffer nbox % kBuffers, nbox counting every box the
+// warpgroup has written), each written out by a TMA tile store that clips rows
+// past N.  The warps arrive on o_empty once their last read of O_t is done.
 template <int DV, int kBuffers>
 __device__ __forceinline__ void write_out_tile(uint32_t tO, uint32_t stage, int r, int lane,
                                                float inv, const CUtensorMap* omap, int qt, int bh,
-                                               uint32_t bar_id, uint64_t* o_empty) {
+                                               uint32_t bar_id, uint64_t* o_empty, int& nbox) {
   const uint32_t sw = static_cast<uint32_t>(r & 7);
 #pragma unroll
   for (int b = 0; b < DV / 32; ++b) {
@@ -206,7 +231,8 @@ __device__ __forceinline__ void write_out_tile(uint32_t tO, uint32_t stage, int 
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty);
     }
-    const uint32_t box = stage + (b % kBuffers) * kBoxBytes;
+    const uint32_t box = stage + (nbox % kBuffers) * kBoxBytes;
+    ++nbox;
     if (r == 0) bulk_wait_group_read<kBuffers - 1>();  // this buffer's last store has read it
     named_bar_sync(bar_id, 128);
     const uint32_t rb = box + r * 128;
@@ -235,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
+  __shared__ float stat_l[2][2][kTileRows], stat_m[2][2][kTileRows];  // [tile][parity][row]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = p.BH * ((p.NT + 1) >> 1);
@@ -257,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.s_full[t], 1);
       mbar_init(&bars.p_full[t], 4);   // one arrival per softmax warp
       mbar_init(&bars.o_final[t], 1);
-      mbar_init(&bars.o_empty[t], 4);  // one arrival per softmax warp
+      mbar_init(&bars.o_empty[t], 4);  // one arrival per output warp
+      mbar_init(&bars.stats_full[t], 4);  // one arrival per softmax warp
     }
     mbar_init(&bars.drain, 1);
     abort_sh = 0;
@@ -267,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base_sh;
-  if (warp >= 8) {
-   setmaxnreg_dec<RegSplit<KD>::kControl>();  // the whole control warpgroup
+  if (warp >= 12) {
+   setmaxnreg_dec<RegSplit::kControl>();  // the whole control warpgroup
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0)
@@ -285,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV = smem_desc(sbase + Plan::kV, 16384, 1024, kLayoutSwizzle128);
       bool first_s0 = true;
       auto issue_s = [&](int t, int slot) {  // S_t = Q_t K_slot^T, then signal the softmax
-        const uint64_t a = dQ0 + static_cast<uint64_t>((t * Plan::kQBytes) >> 4);
-        const uint64_t b = dK + static_cast<uint64_t>((slot * Plan::kKBytes) >> 4);
-        const uint32_t d = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
+        const uint64_t a = opaque64(dQ0) + static_cast<uint64_t>((t * Plan::kQBytes) >> 4);
+        const uint64_t b = opaque64(dK) + static_cast<uint64_t>((slot * Plan::kKBytes) >> 4);
+        const uint32_t d = opaque32(tb) + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
 #pragma unroll
         for (int k = 0; k < KD / 16; ++k)
           mma_ss(d, a + (k * 4096 >> 4), b + (k * 4096 >> 4), kIdescS, k > 0);
@@ -297,9 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) first_s0 = false;
       };
       auto issue_pv = [&](int t, int slot, uint32_t acc) {  // O_t += P_t V_slot
-        const uint32_t a = tb + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
-        const uint32_t d = tb + (t == 0 ? Plan::kColsO0 : Plan::kColsO1);
-        const uint64_t b = dV + static_cast<uint64_t>((slot * Plan::kVBytes) >> 4);
+        const uint32_t a = opaque32(tb) + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
+        const uint32_t d = opaque32(tb) + (t == 0 ? Plan::kColsO0 : Plan::kColsO1);
+        const uint64_t b = opaque64(dV) + static_cast<uint64_t>((slot * Plan::kVBytes) >> 4);
         mma_ts(d, a, b, kIdescPV, acc);
 #pragma unroll
         for (int k = 1; k < 8; ++k) mma_ts(d, a + k * 8, b + (k * 2048 >> 4), kIdescPV, 1u);
@@ -373,47 +401,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars.drain);
       mbar_wait(&bars.drain, 0, ctl.limit_ns);  // own MMAs in flight
     }
-   }  // warps 10-11: no role
+   }  // warps 14-15: no role
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ output
+    setmaxnreg_dec<RegSplit::kOutput>();
+    const int r = tid & 127;
+    const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    int nd0 = 0, nd1 = 0, nbox = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int w = item_index(k, items);
+      if (w < 0) break;
+      const Item it = decode_item(p, w);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? it.nkv0 : it.nkv1) == 0) continue;
+        const int nd = t == 0 ? nd0 : nd1;
+        __syncwarp();
+        ok = named_bar_and(kOutBar, 128,
+                           wait_or_abort(&bars.o_final[t], nd & 1, ctl) &&
+                               wait_or_abort(&bars.stats_full[t], nd & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        const float l = stat_l[t][nd & 1][r], mr = stat_m[t][nd & 1][r];
+        const int qt = it.qt0 + t;
+        if (p.lse != nullptr) {  // log-sum-exp of the row's logits, natural log
+          const int row = qt * kTileRows + r;
+          if (row < p.N) p.lse[static_cast<size_t>(it.bh) * p.N + row] = (mr + log2f(l)) * kLn2;
+        }
+        write_out_tile<DV, Plan::kBoxes>(lane_base + (t == 0 ? Plan::kColsO0 : Plan::kColsO1),
+                                         sbase + Plan::kStage, r, lane, 1.f / l, &omap, qt, it.bh,
+                                         kOutBar, &bars.o_empty[t], nbox);
+        if (t == 0) ++nd0; else ++nd1;
+      }
+    }
+    if (r == 0) bulk_wait_group_read<0>();  // the stores have read shared memory
   } else {
-    // ------------------------------------------------------------ softmax + output
-    setmaxnreg_inc<RegSplit<KD>::kSoftmax>();  // the whole softmax warpgroup
+    // ------------------------------------------------------------ softmax
+    setmaxnreg_inc<RegSplit::kSoftmax>();  // the whole softmax warpgroup
     const int t = warp >> 2;  // query tile of this warpgroup
     const int r = tid & 127;  // row within the tile == TMEM lane
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t tS = lane_base + (t == 0 ? Plan::kColsS0 : Plan::kColsS1);
     const uint32_t tO = lane_base + (t == 0 ? Plan::kColsO0 : Plan::kColsO1);
-    const uint32_t bar_id = 1 + t;  // named barrier of this warpgroup
     uint32_t sph = 0;               // s_full phase bit
-    int ndone = 0;                  // output tiles written
+    int ndone = 0;                  // tiles whose statistics were handed over
     auto row_mul = [&](const Item& x) {
       return p.qmul[static_cast<size_t>(x.bh) * p.NT * kTileRows + (x.qt0 + t) * kTileRows + r];
     };
-    // Where the score depth is 32, the next item's row multiplier and first
-    // key-tile multiplier are loaded before this item's output step, so that
-    // their latency does not fall between the output and the next item's
-    // first softmax (measured: +0.3 to +0.8% at m = 32; at the other depths
-    // the extra live registers cost more than that, and they load in place).
-    constexpr bool kAhead = KD == 32;
-    float qm_next = 0.f, km_next = 0.f;
-    bool pre = false;
     for (int k = 0;; ++k) {
       const int w = item_index(k, items);
       if (w < 0) break;
       const Item it = decode_item(p, w);
       const int nkv_t = t == 0 ? it.nkv0 : it.nkv1;
-      if (nkv_t == 0) {
-        pre = false;
-        continue;
-      }
+      if (nkv_t == 0) continue;
       const int qt = it.qt0 + t;
       const float* kmul = p.kmul + static_cast<size_t>(it.bh) * p.NT;
-      const float qm = (kAhead && pre) ? qm_next : row_mul(it);
-      const float km0 = kAhead ? (pre ? km_next : __ldg(kmul)) : 0.f;
-      pre = false;
+      const float qm = row_mul(it);
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nkv_t; ++j) {
-        const float km = (kAhead && j == 0) ? km0 : __ldg(kmul + j);
+        const float km = __ldg(kmul + j);
         // warp-uniform outcome, so that the warp stays converged for the
         // .sync.aligned tensor-memory instructions below
         if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars.s_full[t], sph, ctl))))
@@ -534,36 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full[t]);
       }
-      if (kAhead && ok) {
-        const int wn = item_index(k + 1, items);
-        if (wn >= 0) {
-          const Item itn = decode_item(p, wn);
-          if ((t == 0 ? itn.nkv0 : itn.nkv1) > 0) {
-            qm_next = row_mul(itn);
-            km_next = __ldg(p.kmul + static_cast<size_t>(itn.bh) * p.NT);
-            pre = true;
-          }
-        }
-      }
-      // ---- output: O / l -> out (fp32) through shared memory and TMA stores.
-      // The whole warpgroup decides together, so that it meets the named
-      // barriers below as one; a thread that gave up has set abort_sh.
-      __syncwarp();
-      ok = named_bar_and(bar_id, 128,
-                         ok && wait_or_abort(&bars.o_final[t], ndone & 1, ctl));
       if (!ok) break;
-      tc_fence_after();
-      const float inv = 1.f / l_run;
-      if (p.lse != nullptr) {  // log-sum-exp of the row's logits, natural log
-        const int row = qt * kTileRows + r;
-        if (row < p.N) p.lse[static_cast<size_t>(it.bh) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
-      }
-      write_out_tile<DV, Plan::kBoxesPerTile>(
-          tO, sbase + Plan::kStage + t * Plan::kBoxesPerTile * kBoxBytes, r, lane, inv, &omap, qt,
-          it.bh, bar_id, &bars.o_empty[t]);
+      // the row's statistics for the output warpgroup, which writes O_t / l
+      stat_l[t][ndone & 1][r] = l_run;
+      stat_m[t][ndone & 1][r] = m_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.stats_full[t]);
       ++ndone;
     }
-    if (r == 0) bulk_wait_group_read<0>();  // the stores have read shared memory
   }
   tc_fence_before();
   __syncthreads();
