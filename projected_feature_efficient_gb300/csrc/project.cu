@@ -41,6 +41,7 @@
 
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "waits.cuh"
 
 namespace spa {
 namespace {
@@ -68,9 +69,9 @@ __device__ __forceinline__ int range_exponent(float amax) {
 
 // Scale, convert and store row `tid` of a score-operand tile, plus its range
 // multiplier.  Called by all 128 threads of the CTA (it may synchronise them).
-template <int MP, ProjOut MODE>
+template <int MP, ProjOut MODE, class Sync>
 __device__ __forceinline__ void store_tile(const ProjParams& p, float (&acc)[MP], int tile,
-                                           int bh, int which, int tid, float* red) {
+                                           int bh, int which, int tid, float* red, Sync sync) {
   constexpr int KD = MODE == ProjOut::BF16X3 ? 3 * MP : MP;
   const int row = tile * kTileRows + tid;
   if constexpr (MODE == ProjOut::F16ROWS) {
@@ -124,7 +125,7 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, float (&acc)[MP]
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if ((tid & 31) == 0) red[tid >> 5] = amax;
-      __syncthreads();
+      sync();
       amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     }
     const int e = range_exponent(amax);
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(128) project_kernel(const ProjParams p) {
         if (k < m) o[k] = acc[k];
     }
   } else {
-    store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red);
+    store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red, [] { __syncthreads(); });
   }
 }
 
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
     // every thread's accumulator is read before the next GEMM overwrites it
     tc_fence_before();
     __syncthreads();
-    store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red);
+    store_tile<MP, MODE>(p, acc, tile, bh, which, tid, red, [] { __syncthreads(); });
   }
   if (tid == 0 && !ok) {
     atomicExch(p.err, 1);
@@ -382,6 +383,240 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, Plan::kCols);
+}
+
+// ------------------------------------------------------------------ warp-specialised tcgen05 kernel
+// One CTA per SM over a contiguous range of units (tensor, head, 128-row
+// tile), with the roles apart so that the copies never wait for the
+// epilogue:
+//   warps 0-7  two epilogue warpgroups, tile i to warpgroup i % 2: the tile's
+//              accumulator out of TMEM (one row per thread), then the range
+//              exponent, conversion and stores of store_tile
+//   warp  8    loads (one thread): X tiles by TMA into a ring of kSlots
+//   warp  9    TMEM allocation; one thread issues each tile's 128 x MP x d
+//              GEMM into one of four TMEM accumulators (two per epilogue
+//              warpgroup)
+// The loader starts at once; the other warps write P_h^T of every head the
+// range touches (at most kWsHeads) into shared memory and meet before the
+// first GEMM.  Used where m != 32: at m = 64 it measured 158 -> 131 us on
+// C4's projection, at m = 128 251 -> 206 us (C5), at m = 16 126 -> 118 us; at
+// m = 32, where the per-CTA kernel runs three CTAs per SM, it was slower
+// (C3 33.4 -> 37 us) and the per-CTA kernel is kept.
+constexpr int kWsHeads = 3;
+constexpr int kWsEpi = 2;  // epilogue warpgroups: tile i goes to warpgroup i % kWsEpi
+constexpr int kWsThreads = 128 * kWsEpi + 64;
+template <int MP, int DCH>
+struct ProjWsPlan {
+  static constexpr int kCols = MP < 32 ? 32 : MP;   // one accumulator's TMEM columns
+  static constexpr int kAcc = 2 * kWsEpi;           // accumulators: two per epilogue warpgroup
+  static constexpr int kTmem = kAcc * kCols <= 32 ? 32 : kAcc * kCols <= 64 ? 64 : kAcc * kCols <= 128 ? 128 : kAcc * kCols <= 256 ? 256 : 512;
+  static constexpr int kXBox = kTileRows * 64 * 2;  // one 64-column TMA box: 16 KB
+  static constexpr int kXTile = DCH * kXBox;
+  static constexpr int kPT = MP * DCH * 64 * 2;     // one head's P_h^T
+  static constexpr int kMax = 227 * 1024 - 2048;
+  static constexpr int kSlotsFit = (kMax - kWsHeads * kPT) / kXTile;
+  static constexpr bool kOk = kSlotsFit >= 2 && kAcc * kCols <= 512;  // else the per-CTA kernel
+  static constexpr int kSlots = kSlotsFit > 6 ? 6 : kSlotsFit < 2 ? 2 : kSlotsFit;
+  static constexpr int kB = kSlots * kXTile;
+  static constexpr int kBytes = kB + kWsHeads * kPT + 1024;
+};
+
+template <int MP, int DCH, ProjOut MODE>
+__global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjParams p,
+                                                            const __grid_constant__ CUtensorMap xq,
+                                                            const __grid_constant__ CUtensorMap xk) {
+  using namespace ptx;
+  using Plan = ProjWsPlan<MP, DCH>;
+  constexpr int DP = DCH * 64;
+  constexpr int NS = Plan::kSlots;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int NA = Plan::kAcc;
+  constexpr int kLoadW = 4 * kWsEpi, kMmaW = kLoadW + 1;
+  __shared__ uint64_t x_full[NS], x_empty[NS], acc_full[NA], acc_empty[NA], drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float red[kWsEpi][2][4];
+  __shared__ volatile int abort_sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long U = static_cast<long long>(p.nx) * p.BH * p.NT;
+  const long long G = gridDim.x;
+  const long long u0 = blockIdx.x * U / G, u1 = (blockIdx.x + 1) * U / G;
+  auto unit_which = [&](long long u) {
+    return static_cast<int>(u / (static_cast<long long>(p.BH) * p.NT));
+  };
+  auto unit_bh = [&](long long u) { return static_cast<int>((u / p.NT) % p.BH); };
+  auto unit_tile = [&](long long u) { return static_cast<int>(u % p.NT); };
+  // heads of the range in order of first use; a unit's P_h^T buffer is the
+  // index of its head in that list
+  const int h_first = unit_bh(u0) % p.H;
+  const WaitCtl ctl{&abort_sh, p.err, kProjWaitNs};
+
+  if (warp == kMmaW) {
+    tmem_alloc(&tmem_base_sh, Plan::kTmem);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int k = 0; k < NS; ++k) {
+      mbar_init(&x_full[k], 1);
+      mbar_init(&x_empty[k], 1);
+    }
+    for (int k = 0; k < NA; ++k) {
+      mbar_init(&acc_full[k], 1);
+      mbar_init(&acc_empty[k], 4);  // one arrival per warp of the epilogue warpgroup
+    }
+    mbar_init(&drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base_sh;
+  // The loader starts at once; the other warps write P_h^T of every head of
+  // the range meanwhile and meet at a named barrier before the first GEMM.
+  if (warp != kLoadW) {
+  // P_h^T of every head of the range: element (n, k) = P_h[k][n] at
+  // ((k/8)*(MP/8) + n/8)*64 + (n%8)*8 + k%8, rows past d zero
+  if (u0 < u1) {
+    int hs[kWsHeads];
+    int nh = 0, hprev = -1;
+    for (long long v = u0; v < u1 && nh <= kWsHeads; v = (v / p.NT + 1) * p.NT) {
+      const int h = unit_bh(v) % p.H;
+      if (h != hprev) {
+        if (nh < kWsHeads) hs[nh] = h;
+        ++nh;
+        hprev = h;
+      }
+    }
+    constexpr int kVec = MP * DP / 8;  // 16-byte pieces of one P_h^T
+    for (int hh = 0; hh < nh && hh < kWsHeads; ++hh) {
+      const uint4* P = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.P) +
+                                                      static_cast<size_t>(hs[hh]) * p.d * MP);
+      uint16_t* sB = reinterpret_cast<uint16_t*>(smem + Plan::kB + hh * Plan::kPT);
+      // builder index: every thread but the loader warp's
+      for (int e = warp < kLoadW ? tid : tid - 32; e < kVec; e += kWsThreads - 32) {
+        const int k = e / (MP / 8), n0 = (e % (MP / 8)) * 8;
+        const uint4 pv = k < p.d ? __ldg(P + (static_cast<size_t>(k) * MP + n0) / 8)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+        uint16_t* dst = sB + ((k >> 3) * (MP / 8) + (n0 >> 3)) * 64 + (k & 7);
+        const uint32_t w[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dst[(2 * q) * 8] = static_cast<uint16_t>(w[q] & 0xFFFFu);
+          dst[(2 * q + 1) * 8] = static_cast<uint16_t>(w[q] >> 16);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+  }
+    named_bar_sync(15, kWsThreads - 32);
+    tc_fence_after();
+  }
+
+  if (warp == kLoadW) {
+    // ---------------------------------------------------------------- loads
+    if (lane == 0) {
+      for (long long u = u0; u < u1; ++u) {
+        const int i = static_cast<int>(u - u0), slot = i % NS;
+        if (i >= NS && !wait_or_abort(&x_empty[slot], ((i / NS) - 1) & 1, ctl)) break;
+        const CUtensorMap* xmap = unit_which(u) == 0 ? &xq : &xk;
+        uint8_t* dst = smem + slot * Plan::kXTile;
+        mbar_arrive_expect_tx(&x_full[slot], Plan::kXTile);
+#pragma unroll
+        for (int c = 0; c < DCH; ++c)
+          tma_load_3d(dst + c * Plan::kXBox, xmap, c * 64, unit_tile(u) * kTileRows, unit_bh(u),
+                      &x_full[slot]);
+      }
+      // every copy started lands before the CTA's memory is released
+      const long long n = u1 - u0;
+      for (long long i = n > NS ? n - NS : 0; i < n; ++i)
+        mbar_wait(&x_full[i % NS], (i / NS) & 1, ctl.limit_ns);
+    }
+  } else if (warp == kMmaW) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, MP, kFmtBF16, 0, 0);
+      int hslot = 0, hprev = h_first;
+      for (long long u = u0; u < u1; ++u) {
+        const int i = static_cast<int>(u - u0), slot = i % NS, ab = i % NA;
+        const int h = unit_bh(u) % p.H;
+        if (h != hprev) { ++hslot; hprev = h; }
+        if (!wait_or_abort(&x_full[slot], (i / NS) & 1, ctl)) break;
+        if (i >= NA && !wait_or_abort(&acc_empty[ab], ((i / NA) - 1) & 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t sx = smem_u32(smem + slot * Plan::kXTile);
+        const uint32_t sb = smem_u32(smem + Plan::kB + hslot * Plan::kPT);
+#pragma unroll
+        for (int st = 0; st < DP / 16; ++st) {
+          const uint64_t ad = smem_desc(sx + (st >> 2) * Plan::kXBox + (st & 3) * 32, 16, 1024,
+                                        kLayoutSwizzle128);
+          const uint64_t bd = smem_desc(sb + st * 2 * (MP / 8) * 128, (MP / 8) * 128, 128,
+                                        kLayoutInterleave);
+          mma_ss(tb + ab * Plan::kCols, ad, bd, idesc, st > 0);
+        }
+        mma_commit(&x_empty[slot]);  // the X tile is read
+        mma_commit(&acc_full[ab]);
+      }
+      mma_commit(&drain);
+      mbar_wait(&drain, 0, ctl.limit_ns);  // own MMAs in flight
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int eg = warp >> 2;  // this epilogue warpgroup takes units eg, eg + kWsEpi, ...
+    const int et = tid & 127;
+    for (long long u = u0 + eg; u < u1; u += kWsEpi) {
+      const int i = static_cast<int>(u - u0), ab = i % NA;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&acc_full[ab], (i / NA) & 1, ctl))) break;
+      tc_fence_after();
+      float acc[MP];
+#pragma unroll
+      for (int c = 0; c < MP; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(tb + ab * Plan::kCols + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[c + q] = __uint_as_float(r[q]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);  // the accumulator may take unit i+2
+      const uint32_t bar = 1 + eg;
+      store_tile<MP, MODE>(p, acc, unit_tile(u), unit_bh(u), unit_which(u), et,
+                           red[eg][(i / kWsEpi) & 1], [bar] { named_bar_sync(bar, 128); });
+    }
+  }
+  if (tid == 0 && abort_sh) atomicExch(p.err, 1);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaW) tmem_dealloc(tb, Plan::kTmem);
+}
+
+template <int MP, int DCH, ProjOut MODE>
+cudaError_t launch_ws_one(const ProjParams& p, cudaStream_t stream) {
+  using Plan = ProjWsPlan<MP, DCH>;
+  auto kern = project_ws_kernel<MP, DCH, MODE>;
+  const int smem = Plan::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long units = static_cast<long long>(p.nx) * p.BH * p.NT;
+  const long long grid = units < sms ? units : sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<unsigned>(grid), kWsThreads, smem, stream>>>(p, p.xmap[0], p.xmap[1]);
+  return cudaGetLastError();
+}
+
+// Whether every CTA's range of units touches at most kWsHeads heads.
+bool project_ws_fits(const ProjParams& p, int sms) {
+  const long long units = static_cast<long long>(p.nx) * p.BH * p.NT;
+  if (units <= 0 || sms <= 0) return false;
+  const long long G = units < sms ? units : sms;
+  const long long per = (units + G - 1) / G;
+  return per / p.NT + 2 <= kWsHeads;
 }
 
 template <typename T, int MP, ProjOut MODE>
@@ -435,6 +670,18 @@ cudaError_t launch_tc_one(const ProjParams& p, cudaStream_t stream) {
 
 template <int MP, ProjOut MODE>
 cudaError_t launch_tc_mp(const ProjParams& p, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      MP != 32 && project_ws_fits(p, sms)) {
+    switch ((p.d + 63) / 64) {
+      case 1: if constexpr (ProjWsPlan<MP, 1>::kOk) return launch_ws_one<MP, 1, MODE>(p, stream); break;
+      case 2: if constexpr (ProjWsPlan<MP, 2>::kOk) return launch_ws_one<MP, 2, MODE>(p, stream); break;
+      case 3: if constexpr (ProjWsPlan<MP, 3>::kOk) return launch_ws_one<MP, 3, MODE>(p, stream); break;
+      case 4: if constexpr (ProjWsPlan<MP, 4>::kOk) return launch_ws_one<MP, 4, MODE>(p, stream); break;
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch ((p.d + 63) / 64) {
     case 1: return launch_tc_one<MP, 1, MODE>(p, stream);
     case 2: return launch_tc_one<MP, 2, MODE>(p, stream);
