@@ -96,6 +96,9 @@ SPA_API int spa_project(const void *x, const void *P, float *x_proj, int B, int 
  *   SPA_BF16: 1 <= d <= 256; m in {16, 32, 64, 128}; d_v in {64, 128}.
  *   SPA_F32 : 1 <= d <= 256; 1 <= m <= 128;          1 <= d_v <= 256.
  *   N up to 2^31 - 1, B*H up to 65535.
+ * Range (SPA_BF16): the softmax accumulates probabilities up to 2^40 times the
+ * row's running maximum between rescales, so the output is finite for value
+ * magnitudes |v| below 2^(87 - log2 N) (2^70 at N = 131072).
  * A workspace of spa_attention_workspace_size() bytes is taken on `stream`
  * from the memory pool the library keeps per device and given back to it on
  * the same stream (SPA_ERR_NOMEM if the allocation fails).  The pool keeps its

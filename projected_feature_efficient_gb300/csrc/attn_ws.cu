@@ -42,10 +42,12 @@
 // +3.3%, C5 +2.0%, bit-identical.)
 //
 // Online softmax (base 2, log2(e)/sqrt(m) already folded into Qp): the
-// running max only moves when a tile's max exceeds it by more than 20; in
-// between, probabilities up to 2^20 are accumulated (finite in bf16 and fp32,
-// same relative precision), which leaves the final O / l unchanged up to
-// rounding and skips almost every rescale of O.
+// running max only moves when a tile's max exceeds it by more than 40; in
+// between, probabilities up to 2^40 are accumulated (bf16 and fp32 keep the
+// same relative precision at any magnitude), which leaves the final O / l
+// unchanged up to rounding and skips almost every rescale of O.  The
+// unnormalised O stays finite for N * 2^40 * max|v| < 2^127, i.e. for values
+// below 2^(87 - log2 N) in magnitude (2^70 at N = 131072).
 //
 // With an `lse` buffer the output warpgroup also writes each row's log-sum-exp
 // (m + log2 l, converted to natural log), which the fused backward uses to
@@ -97,8 +99,8 @@ __device__ __forceinline__ uint32_t opaque32(uint32_t x) {
   asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(x));
   return r;
 }
-constexpr float kRescaleThreshold = 20.f;  // log2 units: p <= 2^20 between rescales
-constexpr float kSumLimit = 1048576.f;     // 2^20: a tile row sum within it bounds every p
+constexpr float kRescaleThreshold = 40.f;        // log2 units: p <= 2^40 between rescales
+constexpr float kSumLimit = 1099511627776.f;     // 2^40: a tile row sum within it bounds every p
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr int kBoxBytes = kTileRows * 128;  // one 128-row x 128-byte output box
 constexpr int kMaxDynSmem = 227 * 1024 - 5 * 1024;  // per-block limit less the static part
@@ -492,13 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c) x[c] = c < kvalid ? x[c] : -INFINITY;
         }
         // The running max m_run moves only when the tile's max exceeds it by
-        // more than the threshold, i.e. when some p would exceed 2^20.  So the
+        // more than the threshold, i.e. when some p would exceed 2^40.  So the
         // first key tile of a row takes the max, and every later one is first
         // exponentiated against m_run; only if the tile's row sum then exceeds
-        // 2^20 (a sum within 2^20 bounds every term) does the warp take the
+        // 2^40 (a sum within 2^40 bounds every term) does the warp take the
         // max and, where it moved, redo the tile from the scores still in
         // registers.  The decisions, and so the bits, are those of taking the
-        // max on every tile (C4 m = 32: 8.33 -> 8.19 ms, C5 16.84 -> 16.46 ms).
+        // max on every tile.  With a margin of 2^20 the redo was frequent
+        // where the logits spread wide (m = 16: a logit standard deviation of
+        // about 11.5 in log2 units at C4, twice m = 32's), and taking the max
+        // on every tile was faster there; with 2^40 the speculative form is
+        // faster at every depth (C4 m = 16 +5.0%, m = 32 +0.6%, C3 +0.7%).
         const float mult = qm * km;  // > 0: range exponents times log2(e)/sqrt(m)
         float alpha = 1.f;
         bool grow = false;
@@ -549,12 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return ls;
         };
-        // (With the split score operands, m = 16, taking the max every time
-        // measured faster: 9.66 against 8.66 ms on C4.)
-        constexpr bool kSpeculate = F16OPS;
-        if (!kSpeculate || j == 0) take_max();
+        if (j == 0) take_max();
         float lsum = exps();
-        if (kSpeculate && j > 0 && __any_sync(0xffffffffu, !(lsum <= kSumLimit))) {
+        if (j > 0 && __any_sync(0xffffffffu, !(lsum <= kSumLimit))) {
           take_max();
           if (__any_sync(0xffffffffu, grow)) lsum = exps();  // rows that did not move: same p
         }

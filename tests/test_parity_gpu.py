@@ -99,6 +99,12 @@ SMALL = [
     (3, 60, 300, 64, 32, 64, True),
     (2, 90, 300, 128, 64, 128, False),
     (2, 80, 260, 64, 16, 64, True),
+    # the warp-specialised projection (m != 32) with several tiles per CTA:
+    # ranges that cross heads and the q/k boundary, the X-tile ring and the
+    # four TMEM accumulators wrapping around
+    (2, 10, 1000, 128, 64, 128, True),
+    (3, 10, 2000, 64, 16, 64, False),
+    (1, 12, 1000, 128, 128, 128, False),
 ]
 
 
