@@ -202,3 +202,27 @@ def test_rows_sum_to_one_through_constant_values():
     assert np.abs(got - 1.0).max() < 2e-2
     max_abs, _ = errors(got, np.ones_like(got))
     assert max_abs < 2e-2
+
+
+@pytest.mark.parametrize("m", [16, 32])
+def test_bf16_large_values_scale_exactly(m):
+    """The softmax accumulates probabilities up to 2^40 times the running max
+    between rescales; the header promises finite results for |v| below
+    2^(87 - log2 N).  Values scaled by 2^60 (exact in bf16, N = 1000 allows
+    up to about 2^77) must give the output scaled by exactly 2^60: every
+    product and sum of the value path scales by the power of two, so the
+    bits match unless something overflowed."""
+    pkg = spa()
+    w = si.WORKLOADS["C2"].scaled(B=1, H=2, N=1000, m=m, causal=True)
+    q, k, v = si.make_qkv(w, seed=73)
+    P = si.make_P(w)
+    dev = torch.device("cuda:0")
+    s = 2.0 ** 60
+    big = (v.double() * s).to(torch.bfloat16)
+    assert torch.equal(big.double() / s, v.double())
+    a = pkg.spa_attention_fwd(q.to(dev), k.to(dev), v.to(dev), P.to(dev), causal=True)
+    b = pkg.spa_attention_fwd(q.to(dev), k.to(dev), big.to(dev), P.to(dev), causal=True)
+    torch.cuda.synchronize()
+    assert pkg.device_error() == 0
+    assert torch.isfinite(b).all()
+    assert torch.equal(b, a * s)
