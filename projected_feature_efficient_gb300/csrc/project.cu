@@ -517,9 +517,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjPar
   if (warp == kLoadW) {
     // ---------------------------------------------------------------- loads
     if (lane == 0) {
+      long long issued = 0;
       for (long long u = u0; u < u1; ++u) {
         const int i = static_cast<int>(u - u0), slot = i % NS;
         if (i >= NS && !wait_or_abort(&x_empty[slot], ((i / NS) - 1) & 1, ctl)) break;
+        ++issued;
         const CUtensorMap* xmap = unit_which(u) == 0 ? &xq : &xk;
         uint8_t* dst = smem + slot * Plan::kXTile;
         mbar_arrive_expect_tx(&x_full[slot], Plan::kXTile);
@@ -529,8 +531,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjPar
                       &x_full[slot]);
       }
       // every copy started lands before the CTA's memory is released
-      const long long n = u1 - u0;
-      for (long long i = n > NS ? n - NS : 0; i < n; ++i)
+      for (long long i = issued > NS ? issued - NS : 0; i < issued; ++i)
         mbar_wait(&x_full[i % NS], (i / NS) & 1, ctl.limit_ns);
     }
   } else if (warp == kMmaW) {
@@ -567,7 +568,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjPar
     const int et = tid & 127;
     for (long long u = u0 + eg; u < u1; u += kWsEpi) {
       const int i = static_cast<int>(u - u0), ab = i % NA;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&acc_full[ab], (i / NA) & 1, ctl))) break;
+      // the warpgroup decides together, so that its four warps meet the
+      // named barrier of store_tile as one (a thread that gave up has set abort_sh)
+      const uint32_t bar = 1 + eg;
+      __syncwarp();
+      if (!named_bar_and(bar, 128, wait_or_abort(&acc_full[ab], (i / NA) & 1, ctl))) break;
       tc_fence_after();
       float acc[MP];
 #pragma unroll
@@ -581,12 +586,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjPar
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);  // the accumulator may take unit i+2
-      const uint32_t bar = 1 + eg;
       store_tile<MP, MODE>(p, acc, unit_tile(u), unit_bh(u), unit_which(u), et,
                            red[eg][(i / kWsEpi) & 1], [bar] { named_bar_sync(bar, 128); });
     }
   }
-  if (tid == 0 && abort_sh) atomicExch(p.err, 1);
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaW) tmem_dealloc(tb, Plan::kTmem);
