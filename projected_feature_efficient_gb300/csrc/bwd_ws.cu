@@ -482,12 +482,13 @@ __device__ __forceinline__ void bwd_gradient(const BwdTcParams& p, uint8_t* smem
                                  pack_f32x2(a4.z, a4.w), pack_f32x2(l4.z, l4.w)),
                        y2, y3);
           float e0 = ex2(y0), e1 = ex2(y1), e2 = ex2(y2), e3 = ex2(y3);
-          if (cmin > 0) {
-            e0 = c < cmin ? 0.f : e0;
-            e1 = c + 1 < cmin ? 0.f : e1;
-            e2 = c + 2 < cmin ? 0.f : e2;
-            e3 = c + 3 < cmin ? 0.f : e3;
-          }
+          // selects without a branch (cmin = 0 keeps every value): a branch per
+          // group of four kept the compiler from interleaving the groups'
+          // exponentials (C4 m=32 +2.0%, C3 +0.6%, m=64 +0.8%)
+          e0 = c < cmin ? 0.f : e0;
+          e1 = c + 1 < cmin ? 0.f : e1;
+          e2 = c + 2 < cmin ? 0.f : e2;
+          e3 = c + 3 < cmin ? 0.f : e3;
           pk[h][2 * i4] = pack_bf16x2(e0, e1);
           pk[h][2 * i4 + 1] = pack_bf16x2(e2, e3);
         }
