@@ -53,9 +53,13 @@ def test_decode_matches_oracle(shape):
         assert np.allclose(got.cpu().numpy(), v[:, :, 0].double().numpy(), rtol=0, atol=1e-6)
 
 
-def test_append_in_pieces_is_bitwise_one_append():
+@pytest.mark.parametrize("m", [32, 64])
+def test_append_in_pieces_is_bitwise_one_append(m):
+    """Appending at any row offset writes the same bits as one append (m = 64
+    goes through the warp-specialised projection kernel, m = 32 through the
+    per-CTA one)."""
     pkg = spa()
-    w = si.WORKLOADS["C3"].scaled(B=2, H=2, N=1500, d=128, m=32, dv=128)
+    w = si.WORKLOADS["C3"].scaled(B=2, H=2, N=1500, d=128, m=m, dv=128)
     q, k, v = si.make_qkv(w, seed=5)
     P = si.make_P(w, seed=6)
     a = build_cache(pkg, k, P, v, 1600)
