@@ -105,6 +105,16 @@ SMALL = [
     (2, 10, 1000, 128, 64, 128, True),
     (3, 10, 2000, 64, 16, 64, False),
     (1, 12, 1000, 128, 128, 128, False),
+    # ... and ranges of five or six tiles over three-tile heads, so that a CTA
+    # stages P_h for three heads (the most that kernel takes)
+    (1, 103, 300, 128, 64, 128, True),
+    (1, 97, 500, 64, 16, 64, False),
+    # its other (m, d) instantiations: one, three and four 64-column boxes of
+    # X per tile (the last with two ring slots at m = 64)
+    (2, 3, 500, 64, 64, 64, True),
+    (1, 2, 300, 192, 16, 128, False),
+    (1, 2, 300, 256, 64, 64, True),
+    (1, 2, 300, 256, 16, 64, False),
 ]
 
 
