@@ -361,6 +361,21 @@ SPA_API int spa_selftest_wait_timeout(int limit_ms);
 SPA_API int spa_selftest_bwd_wait_timeout(int limit_ms);
 
 /*
+ * spa_selftest_proj_wait_timeout -- the same self-test for the tensor-core
+ * projection kernels: the projection stage of a bf16 forward (B=1 H=8 N=4096
+ * d=64, zero inputs; m = 32 runs the per-CTA kernel, m = 64 the
+ * warp-specialised one) in which CTA 0 withholds its first "product done"
+ * arrival and every wait is limited to limit_ms (1..2000).  The waiting
+ * threads give up, the CTA drains its copies and products, frees tensor
+ * memory and sets the device error word; the other CTAs finish normally.
+ * Returns SPA_ERR_TIMEOUT when the kernel reported the timeout (the expected
+ * outcome), SPA_OK when it did not, SPA_ERR_SHAPE for limit_ms out of range,
+ * SPA_ERR_UNSUPPORTED for another m, or another status if a call failed.
+ * The device stays usable afterwards.
+ */
+SPA_API int spa_selftest_proj_wait_timeout(int limit_ms, int m);
+
+/*
  * spa_device_error -- reads and clears the device error word of the current
  * device (synchronising it first).  *code receives 0 when no kernel gave up
  * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.

@@ -48,6 +48,8 @@ lib.spa_selftest_wait_timeout.argtypes = [_i]
 lib.spa_selftest_wait_timeout.restype = _i
 lib.spa_selftest_bwd_wait_timeout.argtypes = [_i]
 lib.spa_selftest_bwd_wait_timeout.restype = _i
+lib.spa_selftest_proj_wait_timeout.argtypes = [_i, _i]
+lib.spa_selftest_proj_wait_timeout.restype = _i
 lib.spa_attention_bwd.argtypes = [_vp] * 10 + [_i] * 8 + [_vp]
 lib.spa_attention_bwd.restype = _i
 lib.spa_host_pool_trim.argtypes = []
@@ -361,6 +363,12 @@ def selftest_wait_timeout(limit_ms: int = 50) -> int:
 def selftest_bwd_wait_timeout(limit_ms: int = 50) -> int:
     """The same self-test for the fused backward kernel (returns the status code)."""
     return int(lib.spa_selftest_bwd_wait_timeout(int(limit_ms)))
+
+
+def selftest_proj_wait_timeout(limit_ms: int = 50, m: int = 64) -> int:
+    """The same self-test for the tensor-core projection kernels (m = 32: the
+    per-CTA kernel, m = 64: the warp-specialised one); returns the status code."""
+    return int(lib.spa_selftest_proj_wait_timeout(int(limit_ms), int(m)))
 
 
 def device_error() -> int:

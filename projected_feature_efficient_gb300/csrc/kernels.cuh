@@ -39,6 +39,8 @@ struct ProjParams {
   int* err;              // device error word
   int out_rows, out_pos; // F16ROWS: rows per (batch, head) of the output, first row written
   void* out_b16[2];      // tile modes, optional: plain bf16 tiles of Xp, [BH][NT][128*m] u16
+  unsigned long long limit_ns;  // tensor-core kernels: time limit of every wait (0: 2 s)
+  int inject_stall;      // failure-detection test only: withhold one barrier arrival
 };
 bool project_tc_eligible(const ProjParams& p);
 cudaError_t launch_project(const ProjParams& p, cudaStream_t stream);

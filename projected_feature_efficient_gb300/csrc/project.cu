@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
   const long long U = static_cast<long long>(p.nx) * p.BH * p.NT;
   const long long G = gridDim.x;
   const long long u0 = blockIdx.x * U / G, u1 = (blockIdx.x + 1) * U / G;
+  const uint64_t lim = p.limit_ns ? p.limit_ns : kProjWaitNs;
 
   // unit -> (tensor, head, tile)
   auto unit_which = [&](long long u) { return static_cast<int>(u / (static_cast<long long>(p.BH) * p.NT)); };
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
       __syncthreads();
       staged_h = h;
     }
-    ok = __syncthreads_and(mbar_wait(&bar_x[slot], (i / NS) & 1, kProjWaitNs));
+    ok = __syncthreads_and(mbar_wait(&bar_x[slot], (i / NS) & 1, lim));
     if (!ok) break;
     if (tid == 0) {
       constexpr uint32_t idesc = idesc_f16(128, MP, kFmtBF16, 0, 0);
@@ -347,10 +348,14 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
                                       kLayoutInterleave);
         mma_ss(tb, ad, bd, idesc, st > 0);
       }
-      mma_commit(&bar_mma);
-      ++commits;
+      // a failure-detection test withholds CTA 0's first "GEMM done": every
+      // thread's wait for it runs out, and the CTA takes its abort path
+      if (!(p.inject_stall && blockIdx.x == 0 && i == 0)) {
+        mma_commit(&bar_mma);
+        ++commits;
+      }
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma, i & 1, kProjWaitNs));
+    ok = __syncthreads_and(mbar_wait(&bar_mma, i & 1, lim));
     if (!ok) break;
     // the GEMM has read X slot `slot`: refill it NS tiles ahead
     if (tid == 0 && u + NS < u1) load(u + NS, slot);
@@ -373,13 +378,13 @@ __global__ void __launch_bounds__(128) project_tc_kernel(const ProjParams p,
     atomicExch(p.err, 1);
     // a GEMM may still be in flight: let it finish before TMEM is released
     mma_commit(&bar_mma);
-    mbar_wait(&bar_mma, commits & 1, kProjWaitNs);
+    mbar_wait(&bar_mma, commits & 1, lim);
   }
   // every X copy started lands before the CTA's memory is released (all of
   // them already have unless a wait gave up): the last copy into each slot
   if (tid == 0)
     for (int i = max(0, issued - NS); i < issued; ++i)
-      mbar_wait(&bar_x[i % NS], (i / NS) & 1, kProjWaitNs);
+      mbar_wait(&bar_x[i % NS], (i / NS) & 1, lim);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, Plan::kCols);
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjPar
   // heads of the range in order of first use; a unit's P_h^T buffer is the
   // index of its head in that list
   const int h_first = unit_bh(u0) % p.H;
-  const WaitCtl ctl{&abort_sh, p.err, kProjWaitNs};
+  const WaitCtl ctl{&abort_sh, p.err, p.limit_ns ? p.limit_ns : kProjWaitNs};
 
   if (warp == kMmaW) {
     tmem_alloc(&tmem_base_sh, Plan::kTmem);
@@ -557,7 +562,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) project_ws_kernel(const ProjPar
           mma_ss(tb + ab * Plan::kCols, ad, bd, idesc, st > 0);
         }
         mma_commit(&x_empty[slot]);  // the X tile is read
-        mma_commit(&acc_full[ab]);
+        // a failure-detection test withholds CTA 0's first "accumulator
+        // ready": its epilogue warpgroup gives up, and every role aborts
+        if (!(p.inject_stall && blockIdx.x == 0 && i == 0)) mma_commit(&acc_full[ab]);
       }
       mma_commit(&drain);
       mbar_wait(&drain, 0, ctl.limit_ns);  // own MMAs in flight

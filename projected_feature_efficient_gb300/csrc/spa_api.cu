@@ -163,12 +163,15 @@ int encode_bf16_rows(CUtensorMap* map, const void* base, int inner, int N, int B
 // Stage 1: projection of q and k into the workspace (and, for the backward,
 // plain bf16 tiles of Qp and Kp into qb, kb in the same pass).
 int run_prepare(const void* q, const void* k, const void* P, int B, int H, int N, int d, int m,
-                int dtype, void* ws, cudaStream_t stream, void* qb = nullptr, void* kb = nullptr) {
+                int dtype, void* ws, cudaStream_t stream, void* qb = nullptr, void* kb = nullptr,
+                unsigned long long limit_ns = 0, int inject_stall = 0) {
   const Layout L = make_layout(B, H, N, m, dtype);
   spa::ProjParams pp = proj_params(q, k, P, B, H, N, d, m, dtype, L, static_cast<char*>(ws));
   pp.use_tc = 1;
   pp.out_b16[0] = qb;
   pp.out_b16[1] = kb;
+  pp.limit_ns = limit_ns;
+  pp.inject_stall = inject_stall;
   if (spa::project_tc_eligible(pp)) {
     int st;
     if ((st = encode_bf16_rows(&pp.xmap[0], q, d, N, B * H))) return st;
@@ -1100,6 +1103,37 @@ int spa_selftest_wait_timeout(int limit_ms) {
   if (!st)
     st = run_apply(buf + ov, reinterpret_cast<float*>(buf + oo), B, H, N, m, dv, 0, SPA_BF16,
                    buf + ow, nullptr, static_cast<unsigned long long>(limit_ms) * 1000000ull, 1);
+  if (!st) st = cuda_status(cudaDeviceSynchronize());
+  int word = 0;
+  if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  if (!st) st = cuda_status(cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  cudaFree(buf);
+  if (st) return st;
+  return word ? SPA_ERR_TIMEOUT : SPA_OK;
+}
+
+int spa_selftest_proj_wait_timeout(int limit_ms, int m) {
+  if (limit_ms <= 0 || limit_ms > 2000) return SPA_ERR_SHAPE;
+  if (m != 32 && m != 64) return SPA_ERR_UNSUPPORTED;
+  // m = 32 runs the per-CTA projection kernel, m = 64 the warp-specialised
+  // one; 512 tiles, so each CTA of either takes one to four of them
+  constexpr int B = 1, H = 8, N = 4096, d = 64;
+  const size_t nq = static_cast<size_t>(B) * H * N * d * 2, np = static_cast<size_t>(H) * d * m * 2;
+  const size_t oq = 0, ok = align256(oq + nq), op = align256(ok + nq), ow = align256(op + np);
+  const size_t total = ow + make_layout(B, H, N, m, SPA_BF16).total;
+  int* err = nullptr;
+  int st = device_error_ptr(&err);
+  if (st) return st;
+  char* buf = nullptr;
+  if (cudaMalloc(reinterpret_cast<void**>(&buf), total) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = cuda_status(cudaMemset(buf, 0, total));  // zero inputs
+  if (!st)
+    st = run_prepare(buf + oq, buf + ok, buf + op, B, H, N, d, m, SPA_BF16, buf + ow, nullptr,
+                     nullptr, nullptr, static_cast<unsigned long long>(limit_ms) * 1000000ull, 1);
   if (!st) st = cuda_status(cudaDeviceSynchronize());
   int word = 0;
   if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));

@@ -60,3 +60,28 @@ def test_backward_kernel_reports_a_withheld_barrier():
         rel = ((g - rr) ** 2).sum() ** 0.5 / ((rr ** 2).sum() ** 0.5)
         assert rel < 1e-2
     assert pkg.device_error() == 0
+
+
+@pytest.mark.parametrize("m", [32, 64])
+def test_projection_kernels_report_a_withheld_barrier(m):
+    """The tensor-core projection kernels' bounded waits (m = 32: the per-CTA
+    kernel, whose 128 threads decide together at each barrier; m = 64: the
+    warp-specialised kernel, whose loader, issuer and two epilogue warpgroups
+    each take their abort path): CTA 0's first "product done" is withheld,
+    its waits give up after 50 ms, and the other CTAs finish normally."""
+    pkg = spa()
+    assert pkg.device_error() == 0
+    t0 = time.perf_counter()
+    status = pkg.selftest_proj_wait_timeout(50, m)
+    elapsed = time.perf_counter() - t0
+    assert status == pkg.SPA_ERR_TIMEOUT, pkg.status_str(status)
+    assert elapsed < 1.5, f"self-test took {elapsed:.2f} s"
+    assert pkg.device_error() == 0
+    # the projection and a whole forward through the same kernel afterwards
+    w = si.WORKLOADS["C3"].scaled(B=1, H=8, N=640, d=64, m=m, dv=64)
+    q, k, v = si.make_qkv(w, seed=11)
+    P = si.make_P(w, seed=12)
+    got = pkg.spa_attention_fwd(q.cuda(), k.cuda(), v.cuda(), P.cuda(), causal=True).cpu().numpy()
+    ref = oracle.attention(q, k, v, P, causal=True)
+    assert_parity(got, ref, w.dtype, "after the projection self-test")
+    assert pkg.device_error() == 0
