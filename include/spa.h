@@ -376,6 +376,23 @@ SPA_API int spa_selftest_bwd_wait_timeout(int limit_ms);
 SPA_API int spa_selftest_proj_wait_timeout(int limit_ms, int m);
 
 /*
+ * spa_selftest_copy_wait_timeout -- the same self-test for the kernels that
+ * wait on their own TMA copies: kernel 0 the fused backward's row statistics
+ * kernel, 1 its tensor-core finish (dq, dk, dP), 2 the SFA Top-k kernel, each
+ * on zero inputs of 8 heads of 4096 rows (d = 64, m = 32, d_v = 128; Top-k on
+ * 128 bf16 features, k = 16).  In kernels 0 and 2 CTA 0 arms its first copy
+ * barrier without starting the copies; in kernel 1 CTA 0 withholds its first
+ * "products done" arrival.  Every wait is limited to limit_ms (1..2000); the
+ * CTA gives up, drains what it started and sets the device error word, and
+ * the other CTAs finish normally.  Returns SPA_ERR_TIMEOUT when the kernel
+ * reported the timeout (the expected outcome), SPA_OK when it did not,
+ * SPA_ERR_SHAPE for limit_ms out of range, SPA_ERR_UNSUPPORTED for another
+ * kernel number, or another status if a call failed.  The device stays usable
+ * afterwards.
+ */
+SPA_API int spa_selftest_copy_wait_timeout(int limit_ms, int kernel);
+
+/*
  * spa_device_error -- reads and clears the device error word of the current
  * device (synchronising it first).  *code receives 0 when no kernel gave up
  * on a bounded wait since the last call, else SPA_ERR_TIMEOUT.

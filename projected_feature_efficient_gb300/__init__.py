@@ -13,6 +13,7 @@ import importlib
 __all__ = [
     "SPA_BF16", "SPA_F32", "SPA_OK", "SPA_ERR_TIMEOUT", "SpaError", "device_error", "lib",
     "lib_path", "selftest_wait_timeout", "selftest_bwd_wait_timeout", "selftest_proj_wait_timeout",
+    "selftest_copy_wait_timeout",
     "spa_attention_fwd", "spa_attention_fwd_host",
     "spa_attention_fwd_ws", "spa_attention_workspace_size", "spa_attention_prepare",
     "spa_attention_apply", "spa_project", "status_str", "kcache_new", "spa_kcache_append",

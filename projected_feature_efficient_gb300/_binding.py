@@ -50,6 +50,8 @@ lib.spa_selftest_bwd_wait_timeout.argtypes = [_i]
 lib.spa_selftest_bwd_wait_timeout.restype = _i
 lib.spa_selftest_proj_wait_timeout.argtypes = [_i, _i]
 lib.spa_selftest_proj_wait_timeout.restype = _i
+lib.spa_selftest_copy_wait_timeout.argtypes = [_i, _i]
+lib.spa_selftest_copy_wait_timeout.restype = _i
 lib.spa_attention_bwd.argtypes = [_vp] * 10 + [_i] * 8 + [_vp]
 lib.spa_attention_bwd.restype = _i
 lib.spa_host_pool_trim.argtypes = []
@@ -369,6 +371,13 @@ def selftest_proj_wait_timeout(limit_ms: int = 50, m: int = 64) -> int:
     """The same self-test for the tensor-core projection kernels (m = 32: the
     per-CTA kernel, m = 64: the warp-specialised one); returns the status code."""
     return int(lib.spa_selftest_proj_wait_timeout(int(limit_ms), int(m)))
+
+
+def selftest_copy_wait_timeout(limit_ms: int = 50, kernel: int = 0) -> int:
+    """The same self-test for the kernels that wait on their own copies
+    (kernel 0: the backward's statistics, 1: its finish, 2: the Top-k);
+    returns the status code."""
+    return int(lib.spa_selftest_copy_wait_timeout(int(limit_ms), int(kernel)))
 
 
 def device_error() -> int:

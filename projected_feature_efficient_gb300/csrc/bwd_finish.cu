@@ -255,8 +255,12 @@ __global__ void __launch_bounds__(kFinThreads, 1) bwd_finish_kernel(
         mma_ss(tb + Plan::kColsDp, smem_desc(sX + k * 2048, kFinBox, 1024, kLayoutSwizzle128),
                smem_desc(sG + k * 2048, kFinBox, 1024, kLayoutSwizzle128), kIdDp,
                (dp_fresh && k == 0) ? 0u : 1u);
-      mma_commit(&bar_mma);
-      ++commits;
+      // a failure-detection test withholds CTA 0's first "products done":
+      // every thread's wait for it runs out, and the CTA takes its abort path
+      if (!(p.inject_stall && blockIdx.x == 0 && i == 0)) {
+        mma_commit(&bar_mma);
+        ++commits;
+      }
     }
     dp_fresh = false;
     ok = __syncthreads_and(mbar_wait(&bar_mma, i & 1, p.limit_ns));

@@ -797,7 +797,7 @@ template <int DV>
 __global__ void __launch_bounds__(128) bwd_stats_tma_kernel(
     const __grid_constant__ CUtensorMap domap, const __grid_constant__ CUtensorMap omap,
     const float* __restrict__ lse, const float* __restrict__ qmul, float* __restrict__ stats,
-    int BH, int N, int NT, float alpha, int* err, unsigned long long limit_ns) {
+    int BH, int N, int NT, float alpha, int* err, unsigned long long limit_ns, int inject_stall) {
   constexpr int kBox = 128 * 128;              // one 128-row x 128-byte box
   constexpr int kDoBoxes = DV / 64, kOBoxes = DV / 32;
   constexpr int kBuf = (kDoBoxes + kOBoxes) * kBox;
@@ -811,12 +811,16 @@ __global__ void __launch_bounds__(128) bwd_stats_tma_kernel(
   auto load = [&](long long blk, int s) {
     const int bh = static_cast<int>(blk / NT), row0 = static_cast<int>(blk % NT) * kTileRows;
     mbar_arrive_expect_tx(&full[s], kBuf);
+    // a failure-detection test arms CTA 0's first buffer without starting its
+    // copies: the wait for it runs out, and nothing is left in flight
+    if (!(inject_stall && blockIdx.x == 0 && s == 0 && issued0 == 0)) {
 #pragma unroll
-    for (int h = 0; h < kDoBoxes; ++h)
-      tma_load_3d(sptr + s * kBuf + h * kBox, &domap, h * 64, row0, bh, &full[s]);
+      for (int h = 0; h < kDoBoxes; ++h)
+        tma_load_3d(sptr + s * kBuf + h * kBox, &domap, h * 64, row0, bh, &full[s]);
 #pragma unroll
-    for (int h = 0; h < kOBoxes; ++h)
-      tma_load_3d(sptr + s * kBuf + (kDoBoxes + h) * kBox, &omap, h * 32, row0, bh, &full[s]);
+      for (int h = 0; h < kOBoxes; ++h)
+        tma_load_3d(sptr + s * kBuf + (kDoBoxes + h) * kBox, &omap, h * 32, row0, bh, &full[s]);
+    }
     if (s == 0) ++issued0;
     else ++issued1;
   };
@@ -915,7 +919,8 @@ cudaError_t launch_bwd_stats_tma(const BwdStatsMaps& mp, const float* lse, const
   const long long nblocks = static_cast<long long>(BH) * NT;
   const long long cap = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
   kern<<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), 128, kSmem, stream>>>(
-      mp.domap, mp.omap, lse, qmul, stats, BH, N, NT, alpha, mp.err, mp.limit_ns);
+      mp.domap, mp.omap, lse, qmul, stats, BH, N, NT, alpha, mp.err, mp.limit_ns,
+      mp.inject_stall);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,7 @@ struct TopkParams {
   CUtensorMap xmap, ymap;
   int* err;       // device error word (a bounded wait that ran out)
   unsigned long long limit_ns;
+  int inject_stall;  // failure-detection test only: leave one copy unissued
 };
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_identity(void* P, int H, int d, int bf16, cudaStream_t stream);  // P[h] = I_d
@@ -122,6 +123,7 @@ struct BwdStatsMaps {
   CUtensorMap domap, omap;
   int* err;                     // device error word
   unsigned long long limit_ns;  // time limit of every wait in the kernel
+  int inject_stall;             // failure-detection test only: leave one copy unissued
 };
 cudaError_t launch_bwd_stats(const BwdStatsMaps& maps, const float* lse, const float* qmul,
                              float* stats, int BH, int N, int NT, int dv, float alpha,
@@ -140,6 +142,7 @@ struct BwdFinishParams {
   int* err;                  // device error word
   int B, H, N, NT, d, m;
   unsigned long long limit_ns;  // time limit of every wait in the kernel
+  int inject_stall;          // failure-detection test only: withhold one barrier arrival
 };
 bool bwd_finish_tc_supported(int d, int m);
 cudaError_t launch_bwd_finish_tc(const BwdFinishParams& p, cudaStream_t stream);

@@ -453,7 +453,8 @@ bool bwd_fused_eligible(int d, int m, int dv, int dtype) {
 // and the bf16 Qp / Kp tiles in it: the zeroed dQp accumulator and the row
 // statistics.
 int bwd_stage_inputs(const float* out, const float* lse, const void* dO, int B, int H, int N,
-                     int d, int m, int d_v, char* w, cudaStream_t stream) {
+                     int d, int m, int d_v, char* w, cudaStream_t stream,
+                     unsigned long long limit_ns = kWaitLimitNs, int inject_stall = 0) {
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
   const int BH = B * H, NT = L.fwd.NT;
   int st;
@@ -468,7 +469,8 @@ int bwd_stage_inputs(const float* out, const float* lse, const void* dO, int B, 
       (st = encode_rows_map(&maps.omap, out, d_v, N, BH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)) ||
       (st = device_error_ptr(&maps.err)))
     return st;
-  maps.limit_ns = kWaitLimitNs;
+  maps.limit_ns = limit_ns;
+  maps.inject_stall = inject_stall;
   return cuda_status(spa::launch_bwd_stats(
       maps, lse, reinterpret_cast<const float*>(w + L.fwd.qmul),
       reinterpret_cast<float*>(w + L.stats), BH, N, NT, d_v, alpha, stream));
@@ -510,7 +512,8 @@ int bwd_stage_kernel(const void* v, const void* dO, float* dv, int B, int H, int
 
 // Fused backward, stage 3: dq, dk and dP from dQp and dKp (one tensor-core pass).
 int bwd_stage_finish(const void* q, const void* k, const void* P, float* dq, float* dk, float* dP,
-                     int B, int H, int N, int d, int m, int d_v, char* w, cudaStream_t stream) {
+                     int B, int H, int N, int d, int m, int d_v, char* w, cudaStream_t stream,
+                     unsigned long long limit_ns = kWaitLimitNs, int inject_stall = 0) {
   const BwdLayout L = make_bwd_layout(B, H, N, d, m, d_v, false);
   const int BH = B * H;
   int st;
@@ -531,7 +534,8 @@ int bwd_stage_finish(const void* q, const void* k, const void* P, float* dq, flo
   fp.NT = L.fwd.NT;
   fp.d = d;
   fp.m = m;
-  fp.limit_ns = kWaitLimitNs;
+  fp.limit_ns = limit_ns;
+  fp.inject_stall = inject_stall;
   return cuda_status(spa::launch_bwd_finish_tc(fp, stream));
 }
 
@@ -689,6 +693,39 @@ int backward_entry(const void* q, const void* k, const void* v, const void* P, c
   const cudaError_t fe = cudaFreeAsync(ws, s);
   if (st) return st;
   return cuda_status(fe);
+}
+
+// The Top-k prologue (spa_topk_features), with the wait limit and the
+// failure-detection injection of the TMA kernel as parameters.
+int topk_features(const void* x, void* y, long long rows, int d, int k, int dtype,
+                  cudaStream_t stream, unsigned long long limit_ns = kWaitLimitNs,
+                  int inject_stall = 0) {
+  if (rows < 0 || d < 0 || k < 0) return SPA_ERR_SHAPE;
+  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
+  if (rows == 0) return SPA_OK;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return SPA_ERR_UNSUPPORTED;
+  if (k < 1 || k > d) return SPA_ERR_SHAPE;
+  if (!x || !y) return SPA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y)) return SPA_ERR_ALIGN;
+  spa::TopkParams tp{};
+  tp.x = x;
+  tp.y = y;
+  tp.rows = rows;
+  tp.d = d;
+  tp.k = k;
+  tp.bf16 = dtype == SPA_BF16;
+  // bf16 rows of 64 or 128 features go through TMA (row coordinates are 32-bit)
+  if (tp.bf16 && (d == 64 || d == 128) && rows <= 0x7fffff00LL) {
+    int st;
+    if ((st = encode_bf16_rows(&tp.xmap, x, d, static_cast<int>(rows), 1)) ||
+        (st = encode_bf16_rows(&tp.ymap, y, d, static_cast<int>(rows), 1)) ||
+        (st = device_error_ptr(&tp.err)))
+      return st;
+    tp.use_tma = 1;
+    tp.limit_ns = limit_ns;
+    tp.inject_stall = inject_stall;
+  }
+  return cuda_status(spa::launch_topk(tp, stream));
 }
 
 }  // namespace
@@ -914,31 +951,7 @@ int spa_attention_decode(const void* q, const void* P, const void* kc, const flo
 
 int spa_topk_features(const void* x, void* y, long long rows, int d, int k, int dtype,
                       void* stream) {
-  if (rows < 0 || d < 0 || k < 0) return SPA_ERR_SHAPE;
-  if (dtype != SPA_F32 && dtype != SPA_BF16) return SPA_ERR_DTYPE;
-  if (rows == 0) return SPA_OK;
-  if (d != 32 && d != 64 && d != 128 && d != 256) return SPA_ERR_UNSUPPORTED;
-  if (k < 1 || k > d) return SPA_ERR_SHAPE;
-  if (!x || !y) return SPA_ERR_NULL;
-  if (!aligned16(x) || !aligned16(y)) return SPA_ERR_ALIGN;
-  spa::TopkParams tp{};
-  tp.x = x;
-  tp.y = y;
-  tp.rows = rows;
-  tp.d = d;
-  tp.k = k;
-  tp.bf16 = dtype == SPA_BF16;
-  // bf16 rows of 64 or 128 features go through TMA (row coordinates are 32-bit)
-  if (tp.bf16 && (d == 64 || d == 128) && rows <= 0x7fffff00LL) {
-    int st;
-    if ((st = encode_bf16_rows(&tp.xmap, x, d, static_cast<int>(rows), 1)) ||
-        (st = encode_bf16_rows(&tp.ymap, y, d, static_cast<int>(rows), 1)) ||
-        (st = device_error_ptr(&tp.err)))
-      return st;
-    tp.use_tma = 1;
-    tp.limit_ns = kWaitLimitNs;
-  }
-  return cuda_status(spa::launch_topk(tp, static_cast<cudaStream_t>(stream)));
+  return topk_features(x, y, rows, d, k, dtype, static_cast<cudaStream_t>(stream));
 }
 
 int spa_sfa_attention_fwd(const void* q, const void* k, const void* v, float* out, int B, int H,
@@ -1134,6 +1147,54 @@ int spa_selftest_proj_wait_timeout(int limit_ms, int m) {
   if (!st)
     st = run_prepare(buf + oq, buf + ok, buf + op, B, H, N, d, m, SPA_BF16, buf + ow, nullptr,
                      nullptr, nullptr, static_cast<unsigned long long>(limit_ms) * 1000000ull, 1);
+  if (!st) st = cuda_status(cudaDeviceSynchronize());
+  int word = 0;
+  if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  if (!st) st = cuda_status(cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  cudaFree(buf);
+  if (st) return st;
+  return word ? SPA_ERR_TIMEOUT : SPA_OK;
+}
+
+int spa_selftest_copy_wait_timeout(int limit_ms, int kernel) {
+  if (limit_ms <= 0 || limit_ms > 2000) return SPA_ERR_SHAPE;
+  if (kernel < 0 || kernel > 2) return SPA_ERR_UNSUPPORTED;
+  // 8 heads of 4096 rows (d = 64, m = 32, d_v = 128): 256 row blocks for the
+  // statistics and the Top-k kernels, 512 tiles for the finish
+  constexpr int B = 1, H = 8, N = 4096, d = 64, m = 32, dv = 128, topk_d = 128, topk_k = 16;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const BwdLayout L = make_bwd_layout(B, H, N, d, m, dv, false);
+  const size_t nx = rows * d * 2, np = static_cast<size_t>(H) * d * m * 2;
+  const size_t ndo = rows * dv * 2, nout = rows * dv * 4, nlse = rows * 4, ng = rows * d * 4;
+  const size_t ndp = static_cast<size_t>(H) * d * m * 4, nt = rows * topk_d * 2;
+  const size_t oq = 0, ok = align256(oq + nx), op = align256(ok + nx), odo = align256(op + np),
+               oo = align256(odo + ndo), ol = align256(oo + nout), odq = align256(ol + nlse),
+               odk = align256(odq + ng), odp = align256(odk + ng), ox = align256(odp + ndp),
+               oy = align256(ox + nt), ow = align256(oy + nt);
+  const size_t total = ow + L.total;
+  int* err = nullptr;
+  int st = device_error_ptr(&err);
+  if (st) return st;
+  char* buf = nullptr;
+  if (cudaMalloc(reinterpret_cast<void**>(&buf), total) != cudaSuccess) {
+    cudaGetLastError();
+    return SPA_ERR_NOMEM;
+  }
+  st = cuda_status(cudaMemset(buf, 0, total));  // zero inputs, statistics and accumulators
+  const unsigned long long lim = static_cast<unsigned long long>(limit_ms) * 1000000ull;
+  char* w = buf + ow;
+  if (!st && kernel == 0)
+    st = bwd_stage_inputs(reinterpret_cast<const float*>(buf + oo),
+                          reinterpret_cast<const float*>(buf + ol), buf + odo, B, H, N, d, m, dv, w,
+                          nullptr, lim, 1);
+  if (!st && kernel == 1)
+    st = bwd_stage_finish(buf + oq, buf + ok, buf + op, reinterpret_cast<float*>(buf + odq),
+                          reinterpret_cast<float*>(buf + odk), reinterpret_cast<float*>(buf + odp),
+                          B, H, N, d, m, dv, w, nullptr, lim, 1);
+  if (!st && kernel == 2)
+    st = topk_features(buf + ox, buf + oy, static_cast<long long>(rows), topk_d, topk_k, SPA_BF16,
+                       nullptr, lim, 1);
   if (!st) st = cuda_status(cudaDeviceSynchronize());
   int word = 0;
   if (!st) st = cuda_status(cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost));

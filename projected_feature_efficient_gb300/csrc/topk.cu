@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(128) topk_rows_bf16_kernel(const uint16_t* __r
 template <int D>
 __global__ void __launch_bounds__(128) topk_rows_bf16_tma_kernel(
     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
-    long long nblocks, int k, int* err, unsigned long long limit_ns) {
+    long long nblocks, int k, int* err, unsigned long long limit_ns, int inject_stall) {
   using namespace ptx;
   constexpr int G = D / 32, V = D / 8, NB = D / 64;  // groups, 16-byte chunks, boxes per row
   constexpr int kBox = 128 * 128;                    // one box: 128 rows x 128 bytes
@@ -305,10 +305,14 @@ __global__ void __launch_bounds__(128) topk_rows_bf16_tma_kernel(
   int issued0 = 0, issued1 = 0;  // thread 0: loads started into buffer 0 / 1
   auto load = [&](long long blk, int s) {
     mbar_arrive_expect_tx(&full[s], kBuf);
+    // a failure-detection test arms CTA 0's first buffer without starting its
+    // copies: the wait for it runs out, and nothing is left in flight
+    if (!(inject_stall && blockIdx.x == 0 && s == 0 && issued0 == 0)) {
 #pragma unroll
-    for (int h = 0; h < NB; ++h)
-      tma_load_3d(sptr + s * kBuf + h * kBox, &xmap, h * 64, static_cast<int>(blk * 128), 0,
-                  &full[s]);
+      for (int h = 0; h < NB; ++h)
+        tma_load_3d(sptr + s * kBuf + h * kBox, &xmap, h * 64, static_cast<int>(blk * 128), 0,
+                    &full[s]);
+    }
     if (s == 0) ++issued0;
     else ++issued1;
   };
@@ -447,7 +451,8 @@ cudaError_t launch_bf16_rows_tma(const TopkParams& p, cudaStream_t stream) {
   const long long nblocks = (p.rows + 127) / 128;
   const long long cap = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
   const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-  kern<<<grid, 128, kSmem, stream>>>(p.xmap, p.ymap, nblocks, p.k, p.err, p.limit_ns);
+  kern<<<grid, 128, kSmem, stream>>>(p.xmap, p.ymap, nblocks, p.k, p.err, p.limit_ns,
+                                     p.inject_stall);
   return cudaGetLastError();
 }
 

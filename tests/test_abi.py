@@ -292,11 +292,14 @@ def test_backward_stages_check_their_workspace(lib):
 
 def test_self_tests_validate_first(lib):
     """The failure-detection self-tests check their arguments before touching
-    the GPU: a time limit outside 1..2000 ms, or an m with no projection kernel
-    to test."""
+    the GPU: a time limit outside 1..2000 ms, or an m or a kernel number with
+    no kernel to test."""
     assert lib.spa_selftest_wait_timeout(0) == SHAPE
     assert lib.spa_selftest_bwd_wait_timeout(2001) == SHAPE
     assert lib.spa_selftest_proj_wait_timeout(0, 64) == SHAPE
     assert lib.spa_selftest_proj_wait_timeout(3000, 32) == SHAPE
     assert lib.spa_selftest_proj_wait_timeout(50, 48) == UNSUPPORTED
     assert lib.spa_selftest_proj_wait_timeout(50, 16) == UNSUPPORTED
+    assert lib.spa_selftest_copy_wait_timeout(0, 0) == SHAPE
+    assert lib.spa_selftest_copy_wait_timeout(50, 3) == UNSUPPORTED
+    assert lib.spa_selftest_copy_wait_timeout(50, -1) == UNSUPPORTED

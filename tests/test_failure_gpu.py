@@ -85,3 +85,39 @@ def test_projection_kernels_report_a_withheld_barrier(m):
     ref = oracle.attention(q, k, v, P, causal=True)
     assert_parity(got, ref, w.dtype, "after the projection self-test")
     assert pkg.device_error() == 0
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2])
+def test_copy_waiting_kernels_report_a_withheld_barrier(kernel):
+    """The kernels that wait on their own TMA copies (0: the fused backward's
+    row statistics, 1: its tensor-core finish, 2: the SFA Top-k): CTA 0 arms a
+    copy barrier without starting the copies (0, 2) or withholds its first
+    "products done" (1); its 128 threads give up together after 50 ms and
+    drain what they started, and the other CTAs finish normally."""
+    pkg = spa()
+    assert pkg.device_error() == 0
+    t0 = time.perf_counter()
+    status = pkg.selftest_copy_wait_timeout(50, kernel)
+    elapsed = time.perf_counter() - t0
+    assert status == pkg.SPA_ERR_TIMEOUT, pkg.status_str(status)
+    assert elapsed < 1.5, f"self-test took {elapsed:.2f} s"
+    assert pkg.device_error() == 0
+    if kernel == 2:  # the Top-k afterwards, bit for bit
+        x = torch.randn((3000, 128), generator=torch.Generator().manual_seed(13)).to(torch.bfloat16)
+        got = pkg.spa_topk_features(x.cuda(), 16).cpu()
+        want = torch.from_numpy(oracle.topk_features(x, 16)).to(torch.bfloat16)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    else:  # a whole fused backward afterwards (statistics, kernel, finish)
+        w = si.WORKLOADS["C3"].scaled(B=1, H=2, N=300, d=64, m=32, dv=128)
+        q, k, v = si.make_qkv(w, seed=15)
+        P = si.make_P(w, seed=16)
+        dO = torch.randn((1, 2, 300, 128), generator=torch.Generator().manual_seed(17)).to(torch.bfloat16)
+        q_, k_, v_, P_, dO_ = (t.cuda() for t in (q, k, v, P, dO))
+        out = pkg.spa_attention_fwd(q_, k_, v_, P_, causal=True)
+        got = pkg.spa_attention_bwd(q_, k_, v_, P_, out, dO_, causal=True)
+        ref = oracle.attention_bwd(q, k, v, P, dO, causal=True)
+        for gg, rr in zip(got, ref):
+            g = gg.cpu().numpy().astype("float64")
+            rel = ((g - rr) ** 2).sum() ** 0.5 / ((rr ** 2).sum() ** 0.5)
+            assert rel < 1e-2
+    assert pkg.device_error() == 0
