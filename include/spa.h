@@ -363,9 +363,10 @@ SPA_API int spa_selftest_bwd_wait_timeout(int limit_ms);
 /*
  * spa_selftest_proj_wait_timeout -- the same self-test for the tensor-core
  * projection kernels: the projection stage of a bf16 forward (B=1 H=8 N=4096
- * d=64, zero inputs; m = 32 runs the per-CTA kernel, m = 64 the
- * warp-specialised one) in which CTA 0 withholds its first "product done"
- * arrival and every wait is limited to limit_ms (1..2000).  The waiting
+ * d=64, zero inputs in buffers taken and released with cudaMalloc/cudaFree;
+ * m = 32 runs the per-CTA kernel, m = 64 the warp-specialised one) in which
+ * CTA 0 withholds its first "product done" arrival and every wait is limited
+ * to limit_ms (1..2000).  The waiting
  * threads give up, the CTA drains its copies and products, frees tensor
  * memory and sets the device error word; the other CTAs finish normally.
  * Returns SPA_ERR_TIMEOUT when the kernel reported the timeout (the expected
@@ -380,7 +381,8 @@ SPA_API int spa_selftest_proj_wait_timeout(int limit_ms, int m);
  * wait on their own TMA copies: kernel 0 the fused backward's row statistics
  * kernel, 1 its tensor-core finish (dq, dk, dP), 2 the SFA Top-k kernel, each
  * on zero inputs of 8 heads of 4096 rows (d = 64, m = 32, d_v = 128; Top-k on
- * 128 bf16 features, k = 16).  In kernels 0 and 2 CTA 0 arms its first copy
+ * 128 bf16 features, k = 16) in buffers taken and released with
+ * cudaMalloc/cudaFree.  In kernels 0 and 2 CTA 0 arms its first copy
  * barrier without starting the copies; in kernel 1 CTA 0 withholds its first
  * "products done" arrival.  Every wait is limited to limit_ms (1..2000); the
  * CTA gives up, drains what it started and sets the device error word, and
